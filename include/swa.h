@@ -1,0 +1,293 @@
+/*
+ * swa.h -- sliding-window grouped-query attention on GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels.  It covers Gemma-3/4-style sliding
+ * layers: prefill (causal or generic mask) into a prompt-sized sliding cache,
+ * compaction at first decode into an anchored buffer of W + 64 rows,
+ * single-token decode under one fixed-shape runtime mask shared by all
+ * sliding layers, and a roll every 64 decode tokens.
+ *
+ * Sources (page title, section):
+ *   [SPYRE]   "Enable compact sliding-window attention for Gemma 3 and Gemma 4
+ *             variants" (torch-spyre/hf-adapters pull request 496), Summary,
+ *             Compilation behavior, Performance.
+ *   [FASTLLM] "Add SDPA attention implementation" (ServiceNow/Fast-LLM pull
+ *             request 512), Summary.
+ *   [BONSAI]  "Gemma3 Local Attention Cache" (jax-ml/bonsai issue 124).
+ *
+ * Conventions (every call):
+ *   - Device pointers belong to the caller.  The library allocates no device
+ *     memory; it owns only the small host-side cache handle.
+ *   - Every call that takes a stream is asynchronous on that stream.
+ *   - Arguments are validated on the host before any CUDA call; a bad call
+ *     returns a status and leaves device memory untouched.
+ *     swa_last_error() then describes the problem (per host thread).
+ *   - Device kernels never trap.  An inconsistency found on the device (a
+ *     corrupted cache state, an image block that crosses a chunk end) is
+ *     recorded in a device error word; swa_cache_check() / swa_plan_check()
+ *     report it as SWA_EDEVICE.
+ *   - bf16 tensors are raw IEEE bfloat16 bits (swa_bf16).  Every tensor
+ *     pointer must be 16-byte aligned.
+ *   - Layouts are row-major with the last dimension contiguous.
+ *
+ * Mask predicate (one sequence, padded positions q and k):
+ *   allowed(q,k) = q >= vs and k >= vs and doc(q) == doc(k) and q - k < W
+ *                  and (k <= q or (img(q) >= 0 and img(q) == img(k)))
+ * i.e. window AND (causal OR same image block) with left padding vs
+ * ([SPYRE] Summary; [FASTLLM] Summary for documents).  The window holds W keys
+ * including the query.  Each image id must form one contiguous run.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SWA_API __attribute__((visibility("default")))
+#else
+#define SWA_API
+#endif
+
+typedef struct CUstream_st* swa_stream_t; /* the same type as cudaStream_t */
+typedef uint16_t swa_bf16;                /* raw bfloat16 bits */
+
+typedef enum swa_status {
+  SWA_OK = 0,
+  SWA_EINVAL = 1,       /* invalid argument (NULL, shape, alignment, size) */
+  SWA_ESTATE = 2,       /* the cache is in the wrong state for this call */
+  SWA_EUNSUPPORTED = 3, /* valid but not supported (head size, group size) */
+  SWA_ECUDA = 4,        /* a CUDA runtime call failed */
+  SWA_ETIMEOUT = 5,     /* a bounded device wait gave up */
+  SWA_EDEVICE = 6       /* an earlier kernel recorded a device-side error */
+} swa_status;
+
+enum { SWA_CACHE_PREFILL = 0, SWA_CACHE_COMPACT = 1 };
+enum { SWA_MODE_CAUSAL = 0, SWA_MODE_GENERIC = 1 };
+enum { SWA_MASK_DECODE = 0, SWA_MASK_PREFILL = 1, SWA_MASK_DENSE_DEBUG = 2 };
+
+/* Rows added to the window by the compact buffer, and the roll period in
+ * decode tokens ("window + 64 anchored buffers", "roll ... every 64 decode
+ * tokens": [SPYRE] Summary). */
+#define SWA_ROLL_ROWS 64
+
+/* ------------------------------------------------------------------------ */
+/* Cache                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Shape of a sliding cache.  One cache holds every sliding layer of a model:
+ * K and V, each [layers, batch, kv_heads, rows, head_dim] bf16.
+ *   kind       SWA_CACHE_PREFILL: prompt-sized, row = position ([SPYRE]
+ *              Summary: prompt-sized sliding caches).
+ *              SWA_CACHE_COMPACT: W + 64 rows, row r holds position origin + r.
+ *   prompt_len S, the padded prompt length (positions 0 .. S-1).
+ *   rows       0 selects the default: max(S, W + 64) for a prefill cache
+ *              (short prompts still get the minimum width, [SPYRE] Summary),
+ *              W + 64 for a compact cache (the only value accepted there).
+ *   window     W >= 1; a compact cache needs W >= 64. */
+typedef struct swa_cache_desc {
+  int32_t kind;
+  int32_t layers;
+  int32_t batch;
+  int32_t kv_heads;
+  int32_t head_dim;
+  int32_t window;
+  int32_t prompt_len;
+  int32_t rows;
+} swa_cache_desc;
+
+/* Device-side cache state (the first 32 bytes of the cache memory).  Kernels
+ * read position data only from here, so one captured graph serves every
+ * decode position ([SPYRE] Compilation behavior: position, origin and
+ * padding travel only in tensor data). */
+typedef struct swa_device_state {
+  int32_t origin;     /* position held by row 0 (compact: S - W at first)   */
+  int32_t next_row;   /* row the next decode step writes                    */
+  int32_t cur_row;    /* row written by the current step (-1 before any)    */
+  int32_t step;       /* decode steps taken                                  */
+  int32_t prompt_len; /* S                                                   */
+  int32_t window;     /* W                                                   */
+  int32_t rows;       /* physical rows per (layer, sequence, head) slab      */
+  int32_t error;      /* first device-side error code, 0 = none              */
+} swa_device_state;
+
+typedef struct swa_cache swa_cache; /* opaque host handle */
+
+/* Bytes of device memory a cache of this shape needs (state + valid_start +
+ * K + V, each part 256-byte aligned).  Returns 0 for an invalid desc. */
+SWA_API size_t swa_cache_bytes(const swa_cache_desc* desc);
+
+/* Bind a cache to caller-owned device memory `dev_mem` (>= swa_cache_bytes,
+ * 256-byte aligned), zero-fill it and write the initial state:
+ *   prefill cache: origin 0, next_row S;   compact cache: origin S - W,
+ *   next_row W (right-aligned anchoring; rows of negative positions stay
+ *   zero and are never admitted by the mask).
+ * dev_valid_start: [batch] int32 device array of left-pad counts (copied),
+ * or NULL for no padding.  On success *out receives a handle the caller frees
+ * with swa_cache_free (which never frees dev_mem). */
+SWA_API swa_status swa_cache_alloc(const swa_cache_desc* desc, void* dev_mem, size_t bytes,
+                                   const int32_t* dev_valid_start, swa_stream_t stream,
+                                   swa_cache** out);
+
+/* Release the host handle only.  NULL is ignored. */
+SWA_API void swa_cache_free(swa_cache* cache);
+
+/* Resolved shape and device pointers of a cache (any out pointer may be NULL):
+ * K and V base pointers ([layers, batch, kv_heads, rows, head_dim] bf16) and
+ * the swa_device_state. */
+SWA_API swa_status swa_cache_info(const swa_cache* cache, swa_cache_desc* desc_out, void** k_out,
+                                  void** v_out, void** state_out);
+
+/* Host mirror of the index map: origin, next_row and decode steps taken. */
+SWA_API swa_status swa_cache_position(const swa_cache* cache, int32_t* origin, int32_t* next_row,
+                                      int32_t* step);
+
+/* Advance the host mirror by `steps` decode steps whose masks were built by
+ * replaying a captured CUDA graph (a replay advances only the device state).
+ * SWA_ESTATE if that would run past a due roll.  No CUDA call. */
+SWA_API swa_status swa_cache_advance(swa_cache* cache, int32_t steps);
+
+/* Synchronise `stream` and report a device-side error recorded in the cache
+ * state (SWA_EDEVICE), clearing it. */
+SWA_API swa_status swa_cache_check(swa_cache* cache, swa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Masks                                                                     */
+/* ------------------------------------------------------------------------ */
+
+/* Description of one prefill call (one chunk of queries).
+ *   batch        B sequences (cache mode), 1 for packed documents.
+ *   seq_len      key positions per sequence: S (cache mode) or the total
+ *                token count T (packed documents).
+ *   chunk_start  first query position of this call ([SPYRE] Summary:
+ *   chunk_len    chunked prefill is preserved); 0 and T for packed documents.
+ *   window       W.
+ *   num_docs     number of packed documents (0 in cache mode).
+ *   valid_start  [B] int32 device, left-pad counts, or NULL (no padding).
+ *   img_id       [B, seq_len] int32 device, -1 for text, the image-block id
+ *                for image tokens, or NULL (text only).  Generic mode only.
+ *                Each id must be one contiguous run inside one chunk.
+ *   cu_seqlens   [num_docs + 1] int32 device document offsets (packed mode,
+ *                [FASTLLM] Summary), or NULL.
+ *   plan         a plan built by swa_build_mask(SWA_MASK_PREFILL) for exactly
+ *                this meta; required by generic-mode prefill. */
+typedef struct swa_prefill_meta {
+  int32_t batch;
+  int32_t seq_len;
+  int32_t chunk_start;
+  int32_t chunk_len;
+  int32_t window;
+  int32_t num_docs;
+  const int32_t* valid_start;
+  const int32_t* img_id;
+  const int32_t* cu_seqlens;
+  const void* plan;
+} swa_prefill_meta;
+
+/* Bytes of the device buffer swa_build_mask(SWA_MASK_PREFILL) fills. */
+SWA_API size_t swa_prefill_plan_bytes(const swa_prefill_meta* meta);
+
+/* Build a runtime mask on the device.
+ * SWA_MASK_DECODE (cache: compact, meta NULL): the per-step decode mask
+ *   [batch, rows] uint8 at dev_out, shared by every sliding layer of the step
+ *   ([SPYRE] Summary: one fixed-shape runtime mask per decode step).  It
+ *   advances the device state: cur_row = next_row, next_row += 1, step += 1,
+ *   and mask[b, r] = (r <= cur_row) and (pos_r > p - W) and
+ *   (pos_r >= valid_start[b]) and (pos_r >= 0), pos_r = origin + r,
+ *   p = S + step (before the increment).  SWA_ESTATE when a roll is due.
+ * SWA_MASK_PREFILL (cache may be NULL, meta required): the prefill plan at
+ *   dev_out (swa_prefill_plan_bytes): for every query row the interval
+ *   [lo, hi] of keys it attends (the predicate above reduces to one interval
+ *   per row), and for every 128-row query tile the key range it touches, so
+ *   the kernel skips key tiles no row needs.  Positions, padding, image
+ *   blocks and documents enter only as device data.
+ * SWA_MASK_DENSE_DEBUG (meta required; meta->plan or causal arithmetic when
+ *   NULL): the dense mask [batch, chunk_len, seq_len] uint8 the prefill kernel
+ *   applies, for tests. */
+SWA_API swa_status swa_build_mask(swa_cache* cache, int32_t kind, const swa_prefill_meta* meta,
+                                  void* dev_out, swa_stream_t stream);
+
+/* Report a device-side error recorded while building `plan` (SWA_EDEVICE,
+ * e.g. an image block crossing the chunk end); synchronises `stream`. */
+SWA_API swa_status swa_plan_check(const void* plan, swa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefill                                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Sliding-window attention for one chunk of queries.
+ * Cache mode (cache = prefill cache): q [B, C, Hq, D]; k, v [B, C, Hkv, D]
+ *   are this chunk's keys/values, written to cache rows
+ *   [chunk_start, chunk_start + C) of `layer` first; attention then reads the
+ *   cache.  k = v = NULL means the rows are already in the cache.
+ * Packed mode (cache = NULL): q [T, Hq, D], k, v [T, Hkv, D]; documents from
+ *   meta->cu_seqlens; mode must be SWA_MODE_GENERIC.
+ * mode SWA_MODE_CAUSAL: the narrow causal plan, img_id must be NULL and no
+ *   plan is needed; SWA_MODE_GENERIC: the generic plan (future same-image
+ *   keys, documents) reads meta->plan ([SPYRE] Compilation behavior).
+ * out [.., Hq, D] bf16 like q; lse (natural-log sum of exp of the scaled
+ *   scores) [.., Hq] fp32, or NULL.  Rows with no admitted key give out = 0
+ *   and lse = -inf.  scale multiplies q.k (typically 1/sqrt(D)).
+ * Supported: head_dim 256 or 512, Hq a multiple of Hkv. */
+SWA_API swa_status swa_prefill(swa_cache* cache, int32_t layer, int32_t mode, int32_t q_heads,
+                               int32_t kv_heads, int32_t head_dim, const swa_prefill_meta* meta,
+                               const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float scale,
+                               swa_bf16* out, float* lse, swa_stream_t stream);
+
+/* Compaction at first decode ([SPYRE] Summary): rows [S - W, S) of every
+ * (layer, sequence, head) slab of the prefill cache go to rows [0, W) of the
+ * compact cache (same shape apart from rows, same S and W); rows of negative
+ * positions are zero.  Bit-exact copy. */
+SWA_API swa_status swa_compact(const swa_cache* prefill, swa_cache* compact, swa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Decode                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes swa_decode needs for this cache and query-head count. */
+SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_heads);
+
+/* One decode token of one sliding layer, after swa_build_mask(DECODE) of the
+ * step: appends k_new, v_new [B, Hkv, D] at the step's row (decode writes go
+ * through the compact cache index, [SPYRE] Summary), then attends q [B, Hq, D]
+ * over the rows the mask [B, rows] admits (decode scans only the compact
+ * allocation, [SPYRE] Compilation behavior).  Split-K over rows, with the last
+ * CTA of each (sequence, kv head) combining the partial results.
+ * out [B, Hq, D] bf16; lse [B, Hq] fp32 or NULL.
+ * workspace: >= swa_decode_workspace_bytes device bytes, zero-filled before
+ * its first use; each call leaves it ready for the next.  Calls that overlap
+ * on the GPU need separate workspaces.
+ * Supported: head_dim 64, 128, 256 or 512; Hq / Hkv in {1, 2, 4, 8}. */
+SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
+                              const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
+                              float scale, swa_bf16* out, float* lse, void* workspace,
+                              size_t ws_bytes, swa_stream_t stream);
+
+/* The roll every 64 decode tokens ([SPYRE] Summary: offset-aware
+ * device-to-device copies): when next_row == rows, rows [64, rows) of every
+ * slab of every layer move to rows [0, W) (an overlap-safe in-place shift),
+ * origin += 64, next_row = W.  SWA_ESTATE unless the roll is due. */
+SWA_API swa_status swa_roll(swa_cache* cache, swa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Message of the last failed call on this host thread ("" if none). */
+SWA_API const char* swa_last_error(void);
+
+/* Static name of a status code. */
+SWA_API const char* swa_status_string(swa_status status);
+
+/* Library ABI version (major * 100 + minor). */
+SWA_API int32_t swa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,141 @@
+// Internal declarations shared by the CUDA translation units of libswa.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "swa.h"
+
+namespace swa {
+
+// Device-side error codes recorded in swa_device_state::error / the plan header.
+enum DevError : int32_t {
+  kErrNone = 0,
+  kErrRowRange = 1,          // decode saw cur_row outside [0, rows)
+  kErrRollDue = 2,           // decode mask built while next_row == rows
+  kErrImageCrossesChunk = 3, // an image block runs past the chunk end
+  kErrBadDocs = 4,           // cu_seqlens does not cover the query rows
+  kErrTimeout = 5,           // a bounded wait inside a kernel gave up
+};
+
+// Query rows per prefill tile; the plan's per-tile key ranges use it.
+constexpr int kPlanBM = 128;
+constexpr int32_t kPlanMagic = 0x53574150;
+
+struct PlanHeader {
+  int32_t magic;
+  int32_t batch;
+  int32_t chunk_start;
+  int32_t chunk_len;
+  int32_t seq_len;
+  int32_t window;
+  int32_t n_qtiles;
+  int32_t error;
+};
+
+// Plan buffer: header (256 B) | row_lo [B*C] | row_hi [B*C] | tile_klo [B*T] | tile_khi [B*T]
+// (T = ceil(C / kPlanBM)); each array starts on a 256-byte boundary.
+struct PlanLayout {
+  size_t off_lo, off_hi, off_tlo, off_thi, total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline PlanLayout plan_layout(int batch, int chunk_len) {
+  PlanLayout p;
+  size_t rows = size_t(batch) * size_t(chunk_len) * sizeof(int32_t);
+  size_t tiles = size_t(batch) * size_t((chunk_len + kPlanBM - 1) / kPlanBM) * sizeof(int32_t);
+  p.off_lo = 256;
+  p.off_hi = p.off_lo + align256(rows);
+  p.off_tlo = p.off_hi + align256(rows);
+  p.off_thi = p.off_tlo + align256(tiles);
+  p.total = p.off_thi + align256(tiles);
+  return p;
+}
+
+// Keys a query at position q attends in the narrow causal plan: the interval
+// [lo, hi] (empty when hi < lo).  Pad queries attend nothing.
+__host__ __device__ inline void causal_interval(int q, int vs, int window, int& lo, int& hi) {
+  if (q < vs) {
+    lo = 0;
+    hi = -1;
+    return;
+  }
+  int a = q - window + 1;
+  lo = a > vs ? a : vs;
+  if (lo < 0) lo = 0;
+  hi = q;
+}
+
+// ---------------------------------------------------------------- launches
+// Each returns the launch's cudaError_t (cudaGetLastError after the launch).
+
+cudaError_t launch_init_state(swa_device_state* st, int32_t* vs_dst, const int32_t* vs_src,
+                              int batch, swa_device_state init, cudaStream_t s);
+
+cudaError_t launch_write_rows(uint16_t* cache_k, uint16_t* cache_v, const uint16_t* k,
+                              const uint16_t* v, int batch, int chunk_len, int kv_heads,
+                              int head_dim, int rows, int layer, int chunk_start, cudaStream_t s);
+
+cudaError_t launch_compact(uint16_t* dk, uint16_t* dv, const uint16_t* sk, const uint16_t* sv,
+                           long long slabs, int src_rows, int dst_rows, int window,
+                           int prompt_len, int head_dim, cudaStream_t s);
+
+cudaError_t launch_roll(uint16_t* k, uint16_t* v, long long slabs, int rows, int window,
+                        int head_dim, swa_device_state* st, cudaStream_t s);
+
+cudaError_t launch_decode_mask(swa_device_state* st, const int32_t* vs, int batch, int rows,
+                               uint8_t* mask, cudaStream_t s);
+
+cudaError_t launch_prefill_plan(const swa_prefill_meta& meta, void* plan, cudaStream_t s);
+
+cudaError_t launch_dense_debug(const swa_prefill_meta& meta, uint8_t* out, cudaStream_t s);
+
+struct DecodeArgs {
+  const uint16_t* q;      // [B, Hq, D]
+  const uint16_t* k_new;  // [B, Hkv, D]
+  const uint16_t* v_new;
+  const uint8_t* mask;    // [B, R]
+  uint16_t* k_cache;      // layer 0 base, [L, B, Hkv, R, D]
+  uint16_t* v_cache;
+  swa_device_state* state;
+  uint16_t* out;          // [B, Hq, D]
+  float* lse;             // [B, Hq] or null
+  int32_t* counters;      // [B * Hkv]
+  float* ws_ml;           // [B, Hq, nsplit, 2]
+  float* ws_acc;          // [B, Hq, nsplit, D]
+  int batch, q_heads, kv_heads, head_dim, rows, layer;
+  int nsplit, rows_per_split;
+  float scale_log2;       // scale * log2(e)
+};
+
+// Split choice and workspace size shared by the host API and the launcher.
+struct DecodeSplit {
+  int nsplit, rows_per_split;
+  size_t off_ml, off_acc, total;
+};
+DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count);
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+struct PrefillArgs {
+  const uint16_t* q;        // [B, C, Hq, D] (packed: [T, Hq, D], B = 1)
+  const uint16_t* k;        // key base: cache layer base or packed keys
+  const uint16_t* v;
+  uint16_t* out;
+  float* lse;
+  const int32_t* valid_start;  // causal mode
+  const void* plan;            // generic mode
+  int batch, chunk_start, chunk_len, q_heads, kv_heads, head_dim, window;
+  long long key_seq_stride;    // elements between sequences' key bases
+  long long key_head_stride;   // elements between kv heads
+  long long key_row_stride;    // elements between key rows
+  int key_rows;                // key rows per sequence (bounds)
+  int generic;
+  float scale_log2;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace swa
