@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -280,6 +281,7 @@ swa_status swa_cache_check(swa_cache* c, swa_stream_t stream) {
   if (err != 0) {
     const int32_t zero = 0;
     cudaMemcpy(&c->state->error, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (err == swa::kErrTimeout) return fail(SWA_ETIMEOUT, "a bounded wait inside a kernel gave up");
     return fail(SWA_EDEVICE, "device error %d recorded in the cache state (%s)", err,
                 err == swa::kErrRowRange  ? "decode row out of range"
                 : err == swa::kErrRollDue ? "decode mask built while a roll was due"
@@ -304,6 +306,7 @@ swa_status swa_plan_check(const void* plan, swa_stream_t stream) {
   if (h.error == swa::kErrImageCrossesChunk)
     return fail(SWA_EDEVICE, "an image block crosses the chunk end (its future keys are not written yet)");
   if (h.error == swa::kErrBadDocs) return fail(SWA_EDEVICE, "cu_seqlens does not cover every token");
+  if (h.error == swa::kErrTimeout) return fail(SWA_ETIMEOUT, "a bounded wait inside a kernel gave up");
   if (h.error != 0) return fail(SWA_EDEVICE, "device error %d recorded in the plan", h.error);
   return SWA_OK;
 }
@@ -397,6 +400,8 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
     a.key_head_stride = slab;
     a.key_row_stride = d.head_dim;
     a.key_rows = meta->chunk_start + meta->chunk_len;
+    a.key_dim_rows = d.rows;
+    a.err = &c->state->error;
   } else {
     if (!meta->cu_seqlens) return fail(SWA_EINVAL, "without a cache, prefill needs packed documents (cu_seqlens)");
     if (mode != SWA_MODE_GENERIC) return fail(SWA_EINVAL, "packed documents use SWA_MODE_GENERIC");
@@ -407,8 +412,10 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
     a.key_head_stride = head_dim;
     a.key_row_stride = (long long)kv_heads * head_dim;
     a.key_rows = meta->seq_len;
+    a.key_dim_rows = meta->seq_len;
+    a.err = reinterpret_cast<int32_t*>(const_cast<void*>(meta->plan)) + offsetof(swa::PlanHeader, error) / 4;
   }
-  cudaError_t e = swa::launch_prefill(a, stream);
+  cudaError_t e = head_dim == 256 ? swa::launch_prefill_tc(a, stream) : swa::launch_prefill_simt(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return SWA_OK;
 }

@@ -72,7 +72,7 @@ decode_kernel(const DecodeArgs a) {
   extern __shared__ float smem[];
   const int sc_len = max(a.rows_per_split, a.nsplit);
   float* sc = smem;                  // [G][sc_len]: scores, then weights, then merge weights
-  float* red = smem + G * sc_len;    // [G][D] cross-warp sum
+  float* red = smem + G * sc_len;    // [warps][G][D] per-warp partial sums (fixed-order reduction)
   __shared__ float s_m[G], s_l[G];
   __shared__ int s_last;
 
@@ -189,7 +189,6 @@ decode_kernel(const DecodeArgs a) {
     }
     __syncthreads();
   }
-  for (int i = tid; i < G * D; i += kDecodeThreads) red[i] = 0.f;
 
   // ---- pass 2: weighted sum of the value rows
   float acc[G][E];
@@ -235,23 +234,25 @@ decode_kernel(const DecodeArgs a) {
     for (int e = 0; e < E; ++e)
 #pragma unroll
       for (int o = LPR; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-  __syncthreads();  // red[] zero-filled
   if (rg == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int j = 0; j < V16; ++j)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) atomicAdd(&red[g * D + (j * LPR + li) * 8 + e], acc[g][j * 8 + e]);
+        for (int e = 0; e < 8; ++e) red[(warp * G + g) * D + (j * LPR + li) * 8 + e] = acc[g][j * 8 + e];
   }
   __syncthreads();
 
-  // ---- partial result of this split
+  // ---- partial result of this split (warps summed in a fixed order: deterministic)
   const int nsplit = a.nsplit;
   const long long head0 = (long long)b * a.q_heads + (long long)h * G;
   for (int i = tid; i < G * D; i += kDecodeThreads) {
     const int g = i / D, d = i % D;
-    a.ws_acc[((head0 + g) * nsplit + split) * D + d] = red[i];
+    float sum = red[i];
+#pragma unroll
+    for (int w = 1; w < kDecodeWarps; ++w) sum += red[w * G * D + i];
+    a.ws_acc[((head0 + g) * nsplit + split) * D + d] = sum;
   }
   if (tid < G) {
     a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 0] = s_m[tid];
@@ -268,19 +269,29 @@ decode_kernel(const DecodeArgs a) {
   __threadfence();
 
   // ---- combine (last CTA of this sequence and kv head)
-  float* wts = sc;  // [G][nsplit] merge weights, reuses the score buffer
+  // split statistics are staged in shared memory with independent loads; the
+  // accumulator loads are issued eight at a time; the summation order over
+  // splits stays fixed (deterministic)
+  float* wts = red;                     // [G][nsplit] merge weights
+  float* sms = red + G * nsplit;        // [G][nsplit] split maxima
+  float* sls = red + 2 * G * nsplit;    // [G][nsplit] split sums
   __shared__ float s_M[G], s_L[G];
+  for (int x = tid; x < G * nsplit; x += kDecodeThreads) {
+    const int g = x / nsplit, s = x % nsplit;
+    sms[x] = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2]);
+    sls[x] = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2 + 1]);
+  }
+  __syncthreads();
   if (tid < G) {
     const int g = tid;
     float M = -CUDART_INF_F;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2]));
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, sms[g * nsplit + s]);
     float Lsum = 0.f;
     for (int s = 0; s < nsplit; ++s) {
-      const float ms = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2]);
-      const float ls = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2 + 1]);
+      const float ms = sms[g * nsplit + s];
       const float w = (ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
       wts[g * nsplit + s] = w;
-      Lsum += w * ls;
+      Lsum += w * sls[g * nsplit + s];
     }
     s_M[g] = M;
     s_L[g] = Lsum;
@@ -288,11 +299,18 @@ decode_kernel(const DecodeArgs a) {
   __syncthreads();
   for (int i = tid; i < G * D; i += kDecodeThreads) {
     const int g = i / D, d = i % D;
+    const float* src = a.ws_acc + (head0 + g) * nsplit * (long long)D + d;
+    const float* w = wts + g * nsplit;
     float o = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
-      const float w = wts[g * nsplit + s];
-      if (w != 0.f) o = fmaf(w, __ldcg(&a.ws_acc[((head0 + g) * nsplit + s) * D + d]), o);
+    int s = 0;
+    for (; s + 8 <= nsplit; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (long long)(s + u) * D);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) o = fmaf(w[s + u], v[u], o);
     }
+    for (; s < nsplit; ++s) o = fmaf(w[s], __ldcg(src + (long long)s * D), o);
     const float L = s_L[g];
     o = L > 0.f ? o / L : 0.f;
     a.out[(head0 + g) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
@@ -307,7 +325,7 @@ decode_kernel(const DecodeArgs a) {
 template <int D, int G>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   const int sc_len = a.rows_per_split > a.nsplit ? a.rows_per_split : a.nsplit;
-  const size_t smem = sizeof(float) * (size_t(G) * sc_len + size_t(G) * D);
+  const size_t smem = sizeof(float) * (size_t(G) * sc_len + size_t(kDecodeWarps) * G * D);
   auto k = decode_kernel<D, G>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));

@@ -131,11 +131,16 @@ struct PrefillArgs {
   long long key_seq_stride;    // elements between sequences' key bases
   long long key_head_stride;   // elements between kv heads
   long long key_row_stride;    // elements between key rows
-  int key_rows;                // key rows per sequence (bounds)
+  int key_rows;                // keys a row may attend lie below this bound
+  int key_dim_rows;            // rows of the key tensor per (sequence, head): Rp or T
   int generic;
   float scale_log2;
+  int32_t* err;                // device error word (cache state or plan header)
 };
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// Tensor-core (tcgen05) prefill, head size 256.
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+// CUDA-core prefill (head size 512).
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s);
 
 }  // namespace swa

@@ -1,6 +1,6 @@
-// Prefill attention, CUDA-core version: one warp per (sequence, query row,
-// query head), online softmax over the row's key interval.  Correct for every
-// mask the plan expresses; it is the bring-up path of the prefill row.
+// Prefill attention on CUDA cores for head size 512: one warp per (sequence,
+// query row, query head), online softmax over the row's key interval.  The
+// head-size-256 path runs on the tensor cores (prefill_sm103.cu).
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
 // variants", Summary and Compilation behavior (narrow causal plan and generic
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(256) prefill_simt_kernel(const PrefillArgs a) 
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
+cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s) {
   const long long warps = (long long)a.batch * a.chunk_len * a.q_heads;
   const long long blocks = (warps * 32 + 255) / 256;
   if (blocks == 0) return cudaSuccess;

@@ -1,0 +1,437 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05), head size 256.
+//
+// One CTA computes 128 query rows of one query head against the key tiles
+// (64 keys each) its rows need -- the tile range comes from the causal
+// arithmetic or from the plan built on the device (generic plan: image
+// blocks, documents).  Warp roles:
+//   warp 0     TMA producer: Q once, then K_j and V_j tiles into a 4-stage
+//              ring of 32 KB slots (128-byte swizzled, 64-column boxes);
+//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
+//              S buffers (16 MMAs of 128x64x16), then O += P_{j-1} V_{j-1}
+//              (4 MMAs of 128x256x16, V read MN-major) into the TMEM O
+//              accumulator; owns the TMEM allocation;
+//   warps 2-5  softmax, one thread per query row (its TMEM lane): load the
+//              S row, apply the row's key interval [lo, hi], online softmax
+//              in the exp2 domain with lazy rescaling of O (only when the row
+//              maximum grows by more than 2^8), write P (bf16) to shared
+//              memory, and finally normalise O and store it.
+// Every wait is bounded; a timeout sets the device error word, makes all
+// roles stop, lets in-flight copies and MMAs finish, and frees TMEM.
+//
+// Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
+// variants", Summary and Compilation behavior (causal square-prefill plan,
+// generic plan for future same-image pairs); "Add SDPA attention
+// implementation", Summary (packed documents, K/V shared by query-head groups).
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+
+namespace swa {
+namespace {
+
+using namespace ptx;
+
+constexpr int BM = kPlanBM;  // 128 query rows per CTA
+constexpr int BN = 64;       // keys per tile
+constexpr int HD = 256;      // head size
+constexpr int NST = 4;       // K/V ring stages
+constexpr int kThreads = 192;
+constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KB
+constexpr int KV_CHUNK = BN * 128;       // one 64-column box of K or V: 8 KB
+constexpr int Q_BYTES = Q_CHUNK * (HD / 64);
+constexpr int KV_BYTES = KV_CHUNK * (HD / 64);
+constexpr int P_BYTES = BM * BN * 2;
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + Q_BYTES;
+constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int N_BARS = 2 * NST + 8;
+constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
+
+constexpr uint32_t TM_O = 0, TM_S0 = HD, TM_S1 = HD + BN, TM_COLS = 512;
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, true);
+constexpr float kRescaleLog2 = 8.f;
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(TM_S1 + BN <= TM_COLS, "TMEM budget");
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t full(int s) const { return base + 8 * s; }
+  __device__ uint32_t empty(int s) const { return base + 8 * (NST + s); }
+  __device__ uint32_t q() const { return base + 8 * (2 * NST); }
+  __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }
+  __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 3 + b); }
+  __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 5 + b); }
+  __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 7); }
+};
+
+// Bounded wait on one phase of an mbarrier.  Gives up when another role has
+// aborted or after kTimeoutNs, recording the timeout.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        if (err) atomicCAS(err, 0, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + OFF_Q, sKV = base + OFF_KV, sP = base + OFF_P;
+  const Bars bars{base + OFF_BAR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_MISC + 4);
+  int32_t* err = a.err;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hq = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int hk = hq / (a.q_heads / a.kv_heads);
+  const int i0 = qt * BM;
+  const int q0 = a.chunk_start + i0;
+
+  // key range [k_lo, k_hi) any row of this tile needs
+  int k_lo = 0, k_hi = 0;
+  if (a.generic) {
+    const PlanLayout L = plan_layout(a.batch, a.chunk_len);
+    const int nqt = (a.chunk_len + BM - 1) / BM;
+    const char* plan = static_cast<const char*>(a.plan);
+    k_lo = reinterpret_cast<const int32_t*>(plan + L.off_tlo)[b * nqt + qt];
+    k_hi = reinterpret_cast<const int32_t*>(plan + L.off_thi)[b * nqt + qt];
+  } else {
+    const int vs = a.valid_start ? a.valid_start[b] : 0;
+    const int qlast = min(q0 + BM - 1, a.chunk_start + a.chunk_len - 1);
+    if (qlast >= vs) {
+      int lo, hi;
+      causal_interval(max(q0, vs), vs, a.window, lo, hi);
+      k_lo = lo;
+      k_hi = qlast + 1;
+    }
+  }
+  k_hi = min(k_hi, a.key_rows);
+  const int kt_lo = k_lo / BN;
+  const int n = (k_hi > k_lo) ? ((k_hi - 1) / BN - kt_lo + 1) : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), 1);
+    }
+    mbar_init(bars.q(), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.s_full(i), 1);
+      mbar_init(bars.p_full(i), 128);
+      mbar_init(bars.pv_done(i), 1);
+    }
+    mbar_init(bars.teardown(), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (n > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bars.q(), Q_BYTES);
+        for (int c = 0; c < HD / 64; ++c) tma_load_4d(sQ + c * Q_CHUNK, &tm_q, bars.q(), 64 * c, i0, hq, b);
+      }
+      __syncwarp();
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const int k0 = (kt_lo + j) * BN;
+        for (int x = 0; x < 2 && ok; ++x) {
+          const int idx = 2 * j + x, s = idx % NST;
+          ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
+          if (ok && lane == 0) {
+            mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
+            const CUtensorMap* m = x ? &tm_v : &tm_k;
+            for (int c = 0; c < HD / 64; ++c)
+              tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), 64 * c, k0, hk, b);
+          }
+          __syncwarp();
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (n > 0) {
+      bool ok = __all_sync(0xffffffffu, wait_bar(bars.q(), 0, abort_flag, err));
+      for (int j = 0; j <= n && ok; ++j) {
+        if (j < n) {
+          const int sb = j & 1, idx = 2 * j, s = idx % NST;
+          bool w = true;
+          if (j >= 2) w = wait_bar(bars.p_full(sb), ((j - 2) >> 1) & 1, abort_flag, err);  // S buffer read
+          w = w && wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err);
+          ok = __all_sync(0xffffffffu, w);
+          if (!ok) break;
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t d = tmem + (sb ? TM_S1 : TM_S0);
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const int c = kk >> 2, sub = kk & 3;
+              const uint64_t ad = sdesc_sw128(sQ + c * Q_CHUNK + sub * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(sKV + s * KV_BYTES + c * KV_CHUNK + sub * 32, 16, 1024);
+              mma_bf16_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(bars.s_full(sb));
+            mma_commit(bars.empty(s));
+          }
+          __syncwarp();
+        }
+        if (j >= 1) {
+          const int i = j - 1, pb = i & 1, idx = 2 * i + 1, s = idx % NST;
+          bool w = wait_bar(bars.p_full(pb), (i >> 1) & 1, abort_flag, err);
+          w = w && wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err);
+          ok = __all_sync(0xffffffffu, w);
+          if (!ok) break;
+          if (lane == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+              const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + kk * 32, 16, 1024);
+              // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
+              // 8-key row groups 1024 B apart
+              const uint64_t bd = sdesc_sw128(sKV + s * KV_BYTES + kk * 2048, KV_CHUNK, 1024);
+              mma_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bars.empty(s));
+            mma_commit(bars.pv_done(pb));
+          }
+          __syncwarp();
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (one row per thread)
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int i = i0 + r;
+    const bool row_ok = i < a.chunk_len;
+    const int q = a.chunk_start + i;
+    int lo = 0, hi = -1;
+    if (row_ok) {
+      if (a.generic) {
+        const PlanLayout L = plan_layout(a.batch, a.chunk_len);
+        const char* plan = static_cast<const char*>(a.plan);
+        lo = reinterpret_cast<const int32_t*>(plan + L.off_lo)[(long long)b * a.chunk_len + i];
+        hi = reinterpret_cast<const int32_t*>(plan + L.off_hi)[(long long)b * a.chunk_len + i];
+      } else {
+        causal_interval(q, a.valid_start ? a.valid_start[b] : 0, a.window, lo, hi);
+      }
+      hi = min(hi, a.key_rows - 1);
+    }
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    float m_run = -CUDART_INF_F, l_run = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int sb = t & 1, pb = t & 1;
+      ok = __all_sync(0xffffffffu, wait_bar(bars.s_full(sb), (t >> 1) & 1, abort_flag, err));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[BN];
+      const uint32_t sAddr = tmem + lane_off + (sb ? TM_S1 : TM_S0);
+      tmem_ld32(sAddr, sr);
+      tmem_ld32(sAddr + 32, sr + 32);
+      tmem_ld_wait();
+      const int k0 = (kt_lo + t) * BN;
+      const bool full = (k0 >= lo) && (k0 + BN - 1 <= hi);
+      float mt = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        float x = __uint_as_float(sr[c]) * a.scale_log2;
+        if (!full && (k0 + c < lo || k0 + c > hi)) x = -CUDART_INF_F;
+        sr[c] = __float_as_uint(x);
+        mt = fmaxf(mt, x);
+      }
+      // lazy rescale: move the reference only when the maximum grows by > 2^8
+      const bool move = (m_run == -CUDART_INF_F) ? (mt > -CUDART_INF_F) : (mt > m_run + kRescaleLog2);
+      const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
+      if (__any_sync(0xffffffffu, rescale)) {
+        ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
+        if (!ok) break;
+        tc_fence_after();
+        const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + TM_O + c0, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tmem + lane_off + TM_O + c0, o);
+        }
+        tmem_st_wait();
+        if (rescale) l_run *= alpha;
+      }
+      if (move) m_run = mt;
+      // probabilities relative to m_run, packed to bf16
+      uint32_t pk[BN / 2];
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN; c += 2) {
+        const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
+        const float p0 = (x0 == -CUDART_INF_F) ? 0.f : exp2f(x0 - m_run);
+        const float p1 = (x1 == -CUDART_INF_F) ? 0.f : exp2f(x1 - m_run);
+        lsum += p0 + p1;
+        pk[c / 2] = pack_bf16(p0, p1);
+      }
+      l_run += lsum;
+      if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
+        ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
+        if (!ok) break;
+      }
+      uint8_t* prow = gbase + OFF_P + pb * P_BYTES + r * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bars.p_full(pb));
+    }
+    // epilogue: O / l -> bf16
+    bool have_o = n > 0 && ok;
+    if (have_o)
+      have_o = __all_sync(0xffffffffu, wait_bar(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
+    tc_fence_after();
+    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * HD;
+    for (int c0 = 0; c0 < HD; c0 += 32) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld32(tmem + lane_off + TM_O + c0, o);
+        tmem_ld_wait();
+      }
+      if (row_ok) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = have_o ? pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv) : 0u;
+        uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      }
+    }
+    if (row_ok && a.lse)
+      a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] =
+          l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let the MMAs and TMA copies this CTA issued finish before TMEM and
+    // shared memory are released
+    if (warp == 1 && lane == 0) {
+      mma_commit(bars.teardown());
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(bars.teardown(), 0) && globaltimer_ns() - t0 < kTimeoutNs) {
+      }
+    }
+    if (warp == 0 && lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 1000000ull) {
+      }
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, TM_COLS);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map with a {64, rows, 1, 1} box and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t box[4] = {64, box_rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+  const uint64_t D = uint64_t(a.head_dim);
+  CUtensorMap mq, mk, mv;
+  // Q / out [B, C, Hq, D]: dims {D, C, Hq, B}
+  const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
+  const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
+  // K / V: dims {D, key rows, Hkv, B} with the caller's strides
+  const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
+  const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
+                          uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
+  if (!make_map(&mq, a.q, qd, qs, BM) || !make_map(&mk, a.k, kd, ks, BN) || !make_map(&mv, a.v, kd, ks, BN))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int nqt = (a.chunk_len + BM - 1) / BM;
+  dim3 grid(a.q_heads, nqt, a.batch);
+  prefill_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace swa

@@ -48,20 +48,28 @@ def run_decode_case(swa, c, check_every_step=True):
     steps = c.steps
     vs = c.valid_start.to(dev)
 
-    pre = swa.Cache(swa.CACHE_PREFILL, 1, B, Hkv, D, W, S, vs)
-    q = (c.prompt_q[0] if c.prompt_q is not None else torch.zeros(B, S, Hq, D, dtype=torch.bfloat16)).to(dev)
-    k = c.prompt_k[0].to(dev).contiguous()
-    v = c.prompt_v[0].to(dev).contiguous()
-    meta = swa.Meta(B, S, 0, S, W, valid_start=vs)
-    out = torch.empty_like(q)
-    lse = torch.empty(B, S, Hq, dtype=torch.float32, device=dev)
-    swa.prefill(pre, 0, swa.MODE_CAUSAL, q, k, v, meta, scale, out, lse)
-    torch.cuda.synchronize()
-    assert np.array_equal(bits(pre.k[0, :, :, :S].transpose(1, 2)), bits(c.prompt_k[0]))
-    assert np.array_equal(bits(pre.v[0, :, :, :S].transpose(1, 2)), bits(c.prompt_v[0]))
-
+    out = lse = None
     cmp_ = swa.Cache(swa.CACHE_COMPACT, 1, B, Hkv, D, W, S, vs)
-    swa.compact(pre, cmp_)
+    if D in (256, 512):
+        # the whole path: prefill into the prompt-sized cache, then compaction
+        pre = swa.Cache(swa.CACHE_PREFILL, 1, B, Hkv, D, W, S, vs)
+        q = (c.prompt_q[0] if c.prompt_q is not None else torch.zeros(B, S, Hq, D, dtype=torch.bfloat16)).to(dev)
+        k = c.prompt_k[0].to(dev).contiguous()
+        v = c.prompt_v[0].to(dev).contiguous()
+        meta = swa.Meta(B, S, 0, S, W, valid_start=vs)
+        out = torch.empty_like(q)
+        lse = torch.empty(B, S, Hq, dtype=torch.float32, device=dev)
+        swa.prefill(pre, 0, swa.MODE_CAUSAL, q, k, v, meta, scale, out, lse)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(pre.k[0, :, :, :S].transpose(1, 2)), bits(c.prompt_k[0]))
+        assert np.array_equal(bits(pre.v[0, :, :, :S].transpose(1, 2)), bits(c.prompt_v[0]))
+        swa.compact(pre, cmp_)
+    else:
+        # prefill supports D = 256 / 512 only: place the prompt's last W positions
+        # in rows [max(0, W - S), W) as compaction would (decode-only head sizes)
+        n = min(S, W)
+        cmp_.k[0, :, :, W - n:W] = c.prompt_k[0, :, S - n:].transpose(1, 2).to(dev)
+        cmp_.v[0, :, :, W - n:W] = c.prompt_v[0, :, S - n:].transpose(1, 2).to(dev)
     model = CompactModel(S, W)
     torch.cuda.synchronize()
     for b in range(B):

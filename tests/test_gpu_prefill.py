@@ -73,7 +73,14 @@ CASES = {
     "vlm_chunked": (4105, 2, 8, 4, 256, 64, 384, 128, 20, {1: [(30, 60), (60, 100), (140, 230), (300, 330)],
                                                           0: [(260, 261)]}),
     "vlm_d512": (4106, 1, 4, 2, 512, 32, 256, 128, 0, {0: [(10, 100), (150, 200)]}),
+    "causal_wide_window": (4108, 1, 2, 1, 256, 2000, 333, 333, 3, None),
+    "causal_window_below_tile": (4109, 2, 2, 2, 256, 20, 200, 72, 11, None),
 }
+
+# query scale that spreads scores over a wide range, so the running maximum of
+# a row keeps growing across key tiles (exercises the rescaling of the output)
+Q_SCALE = {"causal_big_scores": 8.0}
+CASES["causal_big_scores"] = (4110, 2, 4, 2, 256, 300, 400, 400, 9, None)
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -81,6 +88,8 @@ def test_cache_prefill(swa, name):
     seed, B, Hq, Hkv, D, W, S, chunk, max_pad, images = CASES[name]
     c = synth.prefill_case(seed, batch=B, q_heads=Hq, kv_heads=Hkv, head_dim=D, window=W, seq_len=S,
                            chunk=chunk, max_pad=max_pad, images=images)
+    if name in Q_SCALE:
+        c.q = (c.q.float() * Q_SCALE[name]).to(torch.bfloat16)
     for b in range(B):  # pad keys carry finite garbage
         c.k[b, :int(c.valid_start[b])] = 300.0
         c.v[b, :int(c.valid_start[b])] = -300.0
