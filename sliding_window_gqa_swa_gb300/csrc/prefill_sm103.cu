@@ -263,7 +263,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       hi = min(hi, a.key_rows - 1);
     }
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    float m_run = -CUDART_INF_F, l_run = 0.f;
+    // l_run sums the bf16-rounded probabilities (normalises O, which the
+    // tensor core accumulates from the same rounded values); l_exact sums the
+    // unrounded ones (gives the lse)
+    float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const int sb = t & 1, pb = t & 1;
@@ -302,21 +305,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           tmem_st32(tmem + lane_off + TM_O + c0, o);
         }
         tmem_st_wait();
-        if (rescale) l_run *= alpha;
+        if (rescale) {
+          l_run *= alpha;
+          l_exact *= alpha;
+        }
       }
       if (move) m_run = mt;
-      // probabilities relative to m_run, packed to bf16
+      // probabilities relative to m_run, packed to bf16; the row sum adds the
+      // same rounded values the PV product uses, so the output is an exact
+      // convex combination of the admitted value rows
       uint32_t pk[BN / 2];
-      float lsum = 0.f;
+      float lsum = 0.f, esum = 0.f;
 #pragma unroll
       for (int c = 0; c < BN; c += 2) {
         const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
         const float p0 = (x0 == -CUDART_INF_F) ? 0.f : exp2f(x0 - m_run);
         const float p1 = (x1 == -CUDART_INF_F) ? 0.f : exp2f(x1 - m_run);
-        lsum += p0 + p1;
-        pk[c / 2] = pack_bf16(p0, p1);
+        const uint32_t w = pack_bf16(p0, p1);
+        lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        esum += p0 + p1;
+        pk[c / 2] = w;
       }
       l_run += lsum;
+      l_exact += esum;
       if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
         ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
         if (!ok) break;
@@ -355,7 +366,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (row_ok && a.lse)
       a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] =
-          l_run > 0.f ? (m_run + log2f(l_run)) * 0.69314718055994530942f : -CUDART_INF_F;
+          l_exact > 0.f ? (m_run + log2f(l_exact)) * 0.69314718055994530942f : -CUDART_INF_F;
   }
 
   // ------------------------------------------------------------ teardown
