@@ -267,6 +267,31 @@ SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, 
                               float scale, swa_bf16* out, float* lse, void* workspace,
                               size_t ws_bytes, swa_stream_t stream);
 
+/* Largest scratch area swa_decode_noalloc can use (bytes): the device image of
+ * libswa.so holds one static array of this size on every GPU that loads it,
+ * until the process exits. */
+#define SWA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* swa_decode for callers that may not allocate device memory -- for example a
+ * plugin running inside an inference runtime that plans every buffer up front
+ * and hands the plugin only its inputs and outputs, where a cudaMalloc would
+ * break the runtime's memory accounting and can synchronise the device.  The
+ * pages have no counterpart to this entry point; it exists only for such
+ * callers.
+ * Same arguments, results and checks as swa_decode, without the workspace:
+ * the split-K partials live in a static device array of
+ * SWA_DECODE_STATIC_SCRATCH_BYTES.  A shape whose workspace
+ * (swa_decode_workspace_bytes) is larger fails with SWA_EUNSUPPORTED.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Each
+ * call clears the array's ticket counters on `stream` before its kernel.
+ * Every call on a device shares the one array and leaves the last call's
+ * partials in it, so calls that overlap on the GPU (other streams, other host
+ * threads) race: serialise them.  Allocates nothing. */
+SWA_API swa_status swa_decode_noalloc(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
+                                      const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
+                                      float scale, swa_bf16* out, float* lse, swa_stream_t stream);
+
 /* The roll every 64 decode tokens ([SPYRE] Summary: offset-aware
  * device-to-device copies): when next_row == rows, rows [64, rows) of every
  * slab of every layer move to rows [0, W) (an overlap-safe in-place shift),

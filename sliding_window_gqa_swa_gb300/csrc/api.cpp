@@ -499,6 +499,63 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   return SWA_OK;
 }
 
+swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf16* q,
+                              const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask, float scale,
+                              swa_bf16* out, float* lse, swa_stream_t stream) {
+  if (!c) return fail(SWA_EINVAL, "cache is NULL");
+  const swa_cache_desc& d = c->desc;
+  if (d.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "decode needs a compact cache");
+  if (layer < 0 || layer >= d.layers) return fail(SWA_EINVAL, "layer %d out of range", layer);
+  if (q_heads < 1 || q_heads % d.kv_heads) return fail(SWA_EINVAL, "q_heads must be a positive multiple of kv_heads");
+  const int g = q_heads / d.kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return fail(SWA_EUNSUPPORTED, "decode supports Hq/Hkv in {1, 2, 4, 8}");
+  if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256 && d.head_dim != 512)
+    return fail(SWA_EUNSUPPORTED, "decode supports head_dim 64, 128, 256 and 512");
+  if (!q || !k_new || !v_new || !mask || !out) return fail(SWA_EINVAL, "q, k_new, v_new, mask and out are required");
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
+    return fail(SWA_EINVAL, "tensor pointers must be 16-byte aligned");
+  if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
+  if (c->cur_row < 0) return fail(SWA_ESTATE, "build the step's decode mask before decoding");
+  const swa::DecodeSplit sp =
+      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device());
+  if (sp.total > size_t(SWA_DECODE_STATIC_SCRATCH_BYTES))
+    return fail(SWA_EUNSUPPORTED, "this shape needs %zu bytes of decode scratch; the static array holds %zu",
+                sp.total, size_t(SWA_DECODE_STATIC_SCRATCH_BYTES));
+  void* scratch = nullptr;
+  cudaError_t e = swa::decode_static_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+  // the tickets must start at zero
+  e = cudaMemsetAsync(scratch, 0, sp.off_ml, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch tickets)");
+  swa::DecodeArgs a;
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.mask = mask;
+  a.k_cache = c->k;
+  a.v_cache = c->v;
+  a.state = c->state;
+  a.out = out;
+  a.lse = lse;
+  char* ws = static_cast<char*>(scratch);
+  a.counters = reinterpret_cast<int32_t*>(ws);
+  a.ws_ml = reinterpret_cast<float*>(ws + sp.off_ml);
+  a.ws_acc = reinterpret_cast<float*>(ws + sp.off_acc);
+  a.batch = d.batch;
+  a.q_heads = q_heads;
+  a.kv_heads = d.kv_heads;
+  a.head_dim = d.head_dim;
+  a.rows = d.rows;
+  a.layer = layer;
+  a.nsplit = sp.nsplit;
+  a.rows_per_split = sp.rows_per_split;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  e = swa::launch_decode(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return SWA_OK;
+}
+
 swa_status swa_roll(swa_cache* c, swa_stream_t stream) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
   const swa_cache_desc& d = c->desc;

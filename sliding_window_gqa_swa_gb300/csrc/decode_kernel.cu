@@ -19,7 +19,15 @@
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
+#include <mutex>
+
 #include "internal.h"
+
+// Scratch of swa_decode_noalloc (tickets, split statistics, split partials)
+// for callers that cannot allocate device memory.  Every GPU that loads the
+// library holds it until the process exits.  In host code this name is only a
+// host-side stand-in: kernels get the address from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_decode_scratch[SWA_DECODE_STATIC_SCRATCH_BYTES];
 
 namespace swa {
 namespace {
@@ -369,6 +377,24 @@ DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int
   d.off_acc = d.off_ml + align256(ml);
   d.total = d.off_acc + align256(acc);
   return d;
+}
+
+cudaError_t decode_static_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* cached[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with this device current
+    if (e != cudaSuccess) return e;
+    cached[dev] = p;
+  }
+  *ptr = cached[dev];
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {

@@ -119,6 +119,11 @@ DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Device address, on the current device, of the static scratch array that
+// swa_decode_noalloc uses (SWA_DECODE_STATIC_SCRATCH_BYTES); looked up once
+// per device.
+cudaError_t decode_static_scratch(void** ptr);
+
 struct PrefillArgs {
   const uint16_t* q;        // [B, C, Hq, D] (packed: [T, Hq, D], B = 1)
   const uint16_t* k;        // key base: cache layer base or packed keys

@@ -70,6 +70,7 @@ _SIGS = {
     "swa_compact": (_I, [_P, _P, _P]),
     "swa_decode_workspace_bytes": (_SZ, [_P, _I]),
     "swa_decode": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
+    "swa_decode_noalloc": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P]),
     "swa_roll": (_I, [_P, _P]),
     "swa_last_error": (ctypes.c_char_p, []),
     "swa_status_string": (ctypes.c_char_p, [_I]),
