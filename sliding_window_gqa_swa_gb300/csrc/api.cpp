@@ -446,7 +446,8 @@ size_t swa_decode_workspace_bytes(const swa_cache* c, int32_t q_heads) {
     return 0;
   }
   const swa_cache_desc& d = c->desc;
-  return swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device()).total;
+  return swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+                        swa::decode_max_cluster()).total;
 }
 
 swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf16* q,
@@ -469,7 +470,8 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
   if (c->cur_row < 0) return fail(SWA_ESTATE, "build the step's decode mask before decoding");
   const swa::DecodeSplit sp =
-      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device());
+      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+                        swa::decode_max_cluster());
   if (ws_bytes < sp.total) return fail(SWA_EINVAL, "workspace too small (%zu < %zu)", ws_bytes, sp.total);
   swa::DecodeArgs a;
   a.q = q;
@@ -493,6 +495,7 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   a.layer = layer;
   a.nsplit = sp.nsplit;
   a.rows_per_split = sp.rows_per_split;
+  a.cluster = sp.cluster;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -518,7 +521,8 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
   if (c->cur_row < 0) return fail(SWA_ESTATE, "build the step's decode mask before decoding");
   const swa::DecodeSplit sp =
-      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device());
+      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+                        swa::decode_max_cluster());
   if (sp.total > size_t(SWA_DECODE_STATIC_SCRATCH_BYTES))
     return fail(SWA_EUNSUPPORTED, "this shape needs %zu bytes of decode scratch; the static array holds %zu",
                 sp.total, size_t(SWA_DECODE_STATIC_SCRATCH_BYTES));
@@ -550,6 +554,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   a.layer = layer;
   a.nsplit = sp.nsplit;
   a.rows_per_split = sp.rows_per_split;
+  a.cluster = sp.cluster;
   a.scale_log2 = scale * 1.4426950408889634f;
   e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

@@ -1,14 +1,24 @@
-// Single-token decode over the compact cache: append, split-K partial
-// attention and the combine, in one launch.
+// Single-token decode over the compact cache: append, split-K attention and
+// the merge of the splits, in one launch.
 //
-// Grid (nsplit, Hkv, B); each CTA owns a contiguous range of cache rows of
-// one (sequence, kv head) slab and serves all G = Hq / Hkv query heads of the
-// group from every K/V row it loads (grouped-query reuse).  A row is split
-// across LPR lanes so each 16-byte load instruction of a lane group covers a
-// contiguous 128-byte span of the row; rows the runtime mask rejects are
-// never loaded.  Partial (max, sum, accumulator) go to the workspace; the
-// last CTA of each (sequence, kv head) -- found with an atomic ticket, no
-// waiting -- merges them, writes the bf16 output and resets the ticket.
+// Grid (nsplit, Hkv, B).  Each CTA owns a contiguous range of rows of one
+// (sequence, kv head) slab.  A producer warp issues bulk asynchronous copies
+// of the range, in chunks of contiguous rows (32 KB of K + V per chunk), into
+// a 3-stage shared-memory ring: the first chunks at once, later chunks only
+// when the runtime mask admits one of their rows.  It also stages the step's
+// new K/V row (used in place of the cache row it replaces) and appends it to
+// the cache.  Four compute warps each take a quarter of the rows of every
+// chunk and keep their own online-softmax state for all G query heads of the
+// group (each loaded K/V row serves the whole group); a row is split across
+// LPR lanes so a lane group reads a contiguous 128-byte span of it.  The
+// warps are merged in a fixed order.  Then:
+//   * one split: the CTA writes the output;
+//   * a cluster of splits (at most 8): the CTAs of a slab form a thread-block
+//     cluster and rank 0 merges their partials through distributed shared
+//     memory;
+//   * more splits: partials go to the workspace and the last CTA of the slab
+//     (atomic ticket, no waiting) merges them and resets the ticket.
+// The merge order is fixed everywhere, so results are deterministic.
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
 // variants", Summary (decode writes through the compact cache index; one
@@ -22,6 +32,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
 
 // Scratch of swa_decode_noalloc (tickets, split statistics, split partials)
 // for callers that cannot allocate device memory.  Every GPU that loads the
@@ -32,25 +43,38 @@ static __device__ __align__(256) unsigned char g_decode_scratch[SWA_DECODE_STATI
 namespace swa {
 namespace {
 
-constexpr int kDecodeThreads = 128;
-constexpr int kDecodeWarps = kDecodeThreads / 32;
+using namespace ptx;
+
+constexpr int kComputeWarps = 16;
+constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
+constexpr int kStages = 3;
+constexpr int kStageBytes = 32768;                  // K chunk + V chunk
+constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 template <int D, int G>
-struct DecodeShape {
-  static constexpr int kWant = D * G / 64;
-  static constexpr int LPR = kWant < 8 ? 8 : (kWant > 32 ? 32 : kWant);  // lanes per row
-  static constexpr int E = D / LPR;        // elements per lane
-  static constexpr int V16 = E / 8;        // 16-byte vectors per lane per row
-  static constexpr int RPW = 32 / LPR;     // rows per warp pass
-  static constexpr int U = (V16 * 2 <= 8) ? 4 : 2;  // passes in flight
+struct Shape {
+  static constexpr int CH = kStageBytes / (2 * D * 2);  // rows per chunk
+  static constexpr int RPC = CH / kComputeWarps;        // rows per warp per chunk
+  static constexpr int kWant = D * G / 64;              // lanes per row keeping q + acc in registers
+  static constexpr int kMin = 32 / RPC;                 // a warp pass must not exceed its rows
+  static constexpr int kLpr = kWant > kMin ? kWant : kMin;
+  static constexpr int LPR = kLpr < 8 ? 8 : (kLpr > 32 ? 32 : kLpr);  // lanes per row
+  static constexpr int E = D / LPR;                     // elements per lane
+  static constexpr int V16 = E / 8;                     // 16-byte vectors per lane per row
+  static constexpr int RPW = 32 / LPR;                  // rows per warp pass
+  static constexpr int PASSES = RPC / RPW;
+  static_assert(PASSES >= 1 && RPC % RPW == 0, "chunk shape");
 };
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+// Shared-memory slots the warp merge uses: as many as fit in the ring next
+// to the CTA accumulator and the combine's statistics (a power of two that
+// divides the warp count).
+__host__ __device__ constexpr int merge_slots(int g, int d) {
+  return (kComputeWarps + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps
+         : (kComputeWarps / 2 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 2
+         : (kComputeWarps / 4 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 4
+         : (kComputeWarps / 8 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 8
+                                                                                        : 1;
 }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
@@ -62,209 +86,435 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   }
 }
 
-template <int D, int G>
-__global__ void __launch_bounds__(kDecodeThreads)
-decode_kernel(const DecodeArgs a) {
-  using S = DecodeShape<D, G>;
-  constexpr int LPR = S::LPR, E = S::E, V16 = S::V16, RPW = S::RPW, U = S::U;
-  constexpr int ROWS_PER_PASS = kDecodeWarps * RPW;
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicCAS(err, 0, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
 
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Shared memory (dynamic): ring [kStages][K chunk | V chunk] (reused after the
+// chunk loop for the per-warp accumulators [warps][G][D], the CTA accumulator
+// [G][D] and the combine's split statistics) | new K row | new V row | mask
+// bytes of the range | chunk flags | barriers.
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_kernel(const DecodeArgs a) {
+  using S = Shape<D, G>;
+  constexpr int LPR = S::LPR, E = S::E, V16 = S::V16, RPW = S::RPW, CH = S::CH, RPC = S::RPC,
+                PASSES = S::PASSES;
+  constexpr int CHUNK_BYTES = CH * D * 2;
+
+  extern __shared__ __align__(128) uint8_t smem[];
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int R = a.rows;
   const int r0 = split * a.rows_per_split;
   const int r1 = min(R, r0 + a.rows_per_split);
   const int nrows = max(0, r1 - r0);
+  const int nchunks = (nrows + CH - 1) / CH;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int li = lane % LPR, rg = lane / LPR;
 
-  extern __shared__ float smem[];
-  const int sc_len = max(a.rows_per_split, a.nsplit);
-  float* sc = smem;                  // [G][sc_len]: scores, then weights, then merge weights
-  float* red = smem + G * sc_len;    // [warps][G][D] per-warp partial sums (fixed-order reduction)
-  __shared__ float s_m[G], s_l[G];
+  uint8_t* kn_s = smem + kStages * kStageBytes;
+  uint8_t* vn_s = kn_s + D * 2;
+  uint8_t* mask_s = vn_s + D * 2;
+  const int mask_bytes = (a.rows_per_split + 15) & ~15;
+  uint8_t* chunk_on = mask_s + mask_bytes;
+  const int flag_bytes = ((a.rows_per_split + CH - 1) / CH + 15) & ~15;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(chunk_on + flag_bytes);  // full[kStages], empty[kStages]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages);
+  __shared__ float s_m[kComputeWarps][G], s_l[kComputeWarps][G];
+  __shared__ float s_M[G], s_L[G];
   __shared__ int s_last;
+  const uint32_t sring = smem_u32(smem);
+  const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kStages);
 
-  const int cur = a.state->cur_row;
-  const bool state_ok = cur >= 0 && cur < R;
-  if (!state_ok && split == 0 && tid == 0) atomicCAS(&a.state->error, 0, kErrRowRange);
-
+  swa_device_state* st = a.state;
   const long long slab = (((long long)a.layer * a.batch + b) * a.kv_heads + h) * (long long)R * D;
   uint16_t* Kc = a.k_cache + slab;
   uint16_t* Vc = a.v_cache + slab;
   const uint16_t* kn = a.k_new + ((long long)b * a.kv_heads + h) * D;
   const uint16_t* vn = a.v_new + ((long long)b * a.kv_heads + h) * D;
-  const uint8_t* mrow = a.mask + (long long)b * R;
-
-  // append the new row (only the CTA whose range holds it)
-  if (state_ok && cur >= r0 && cur < r1) {
-    for (int i = tid; i < D / 8; i += kDecodeThreads) {
-      reinterpret_cast<uint4*>(Kc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(kn)[i];
-      reinterpret_cast<uint4*>(Vc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(vn)[i];
+  const int nspec = min(kStages, nchunks);  // chunks loaded before the mask is known
+  // a range that fits in the ring is loaded at once by every thread with
+  // 16-byte asynchronous copies (lowest latency); longer ranges stream
+  // through the ring with bulk copies
+  const bool oneshot = nchunks <= kStages;
+  if (oneshot) {
+    constexpr int U = D / 8;  // 16-byte units per row
+    const int units = nrows * U;
+    for (int x = tid; x < 2 * units; x += kThreads) {
+      const int kv = x >= units, y = kv ? x - units : x;
+      const int row = y / U, col = y % U;
+      const int c = row / CH, rr = row % CH;
+      const uint32_t dst = sring + c * kStageBytes + kv * CHUNK_BYTES + (rr * U + col) * 16;
+      cp_async_16(dst, (kv ? Vc : Kc) + (long long)(r0 + row) * D + col * 8);
     }
   }
 
-  // this lane's slice of the G query vectors, pre-scaled into the exp2 domain
-  float qr[G][E];
-  {
+  if (warp == kComputeWarps) {
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(bar_full0 + 8 * s, 1);
+        mbar_init(bar_empty0 + 8 * s, kComputeWarps);
+      }
+      *abort_flag = 0;
+      fence_mbar_init();
+      for (int c = 0; c < (oneshot ? 0 : nspec); ++c) {
+        const uint32_t bytes = uint32_t(min(CH, nrows - c * CH)) * D * 2;
+        mbar_arrive_expect_tx(bar_full0 + 8 * c, 2 * bytes);
+        const long long row = r0 + c * CH;
+        bulk_load(sring + c * kStageBytes, Kc + row * D, bytes, bar_full0 + 8 * c);
+        bulk_load(sring + c * kStageBytes + CHUNK_BYTES, Vc + row * D, bytes, bar_full0 + 8 * c);
+      }
+    }
+    // the new row, the mask bytes of the range
+    for (int i = lane; i < D / 8; i += 32) {
+      reinterpret_cast<uint4*>(kn_s)[i] = reinterpret_cast<const uint4*>(kn)[i];
+      reinterpret_cast<uint4*>(vn_s)[i] = reinterpret_cast<const uint4*>(vn)[i];
+    }
+    const uint8_t* mrow = a.mask + (long long)b * R + r0;
+    for (int i = lane; i < nrows; i += 32) mask_s[i] = mrow[i];
+  }
+  // the compute warps fetch their query slices before the first barrier so the
+  // load overlaps the state, mask and K/V round trip
+  uint4 qraw[G][V16];
+  if (warp < kComputeWarps) {
+    const int li = lane % LPR;
     const uint16_t* qp = a.q + ((long long)b * a.q_heads + (long long)h * G) * D;
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int j = 0; j < V16; ++j) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qp + g * D + (j * LPR + li) * 8);
-        float f[8];
-        bf16x8_to_f32(v, f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qr[g][j * 8 + e] = f[e] * a.scale_log2;
-      }
+      for (int j = 0; j < V16; ++j) qraw[g][j] = *reinterpret_cast<const uint4*>(qp + g * D + (j * LPR + li) * 8);
   }
-
-  // ---- pass 1: scores of every row of the range
-  for (int p0 = 0; p0 < nrows; p0 += ROWS_PER_PASS * U) {
-    uint4 kv[U][V16];
-    bool act[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + p0 + u * ROWS_PER_PASS + warp * RPW + rg;
-      act[u] = state_ok && r < r1 && mrow[r] != 0;
-      if (act[u]) {
-        const uint16_t* src = (r == cur) ? kn : Kc + (long long)r * D;
-#pragma unroll
-        for (int j = 0; j < V16; ++j) kv[u][j] = ld_stream(src + (j * LPR + li) * 8);
-      }
+  const int cur = st->cur_row;
+  const bool state_ok = cur >= 0 && cur < R;
+  if (oneshot) cp_async_wait_all();
+  __syncthreads();
+  if (warp == kComputeWarps) {
+    for (int c = lane; c < nchunks; c += 32) {
+      uint8_t any = 0;
+      for (int i = c * CH; i < min(nrows, (c + 1) * CH); ++i) any |= mask_s[i];
+      chunk_on[c] = oneshot || (c < nspec) || (state_ok && any);
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      float s[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] = 0.f;
-      if (act[u]) {
-#pragma unroll
-        for (int j = 0; j < V16; ++j) {
-          float f[8];
-          bf16x8_to_f32(kv[u][j], f);
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) s[g] = fmaf(qr[g][j * 8 + e], f[e], s[g]);
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) s[g] += __shfl_xor_sync(0xffffffffu, s[g], o);
-      const int r = r0 + p0 + u * ROWS_PER_PASS + warp * RPW + rg;
-      if (li == 0 && r < r1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) sc[g * sc_len + (r - r0)] = act[u] ? s[g] : -CUDART_INF_F;
-      }
-    }
+  }
+  if (!state_ok) {
+    if (split == 0 && tid == 0) atomicCAS(&st->error, 0, kErrRowRange);
+    for (int i = tid; i < nrows; i += kThreads) mask_s[i] = 0;
   }
   __syncthreads();
 
-  // ---- softmax statistics of the range (per query head)
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float m = -CUDART_INF_F;
-    for (int i = tid; i < nrows; i += kDecodeThreads) m = fmaxf(m, sc[g * sc_len + i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (tid == 0) {
-      float mm = red[0];
-      for (int w = 1; w < kDecodeWarps; ++w) mm = fmaxf(mm, red[w]);
-      s_m[g] = mm;
-    }
-    __syncthreads();
-    const float mg = s_m[g];
-    float l = 0.f;
-    for (int i = tid; i < nrows; i += kDecodeThreads) {
-      const float x = sc[g * sc_len + i];
-      const float p = (x == -CUDART_INF_F) ? 0.f : exp2f(x - mg);
-      sc[g * sc_len + i] = p;
-      l += p;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    __syncthreads();
-    if (lane == 0) red[warp] = l;
-    __syncthreads();
-    if (tid == 0) {
-      float ll = 0.f;
-      for (int w = 0; w < kDecodeWarps; ++w) ll += red[w];
-      s_l[g] = ll;
-    }
-    __syncthreads();
-  }
-
-  // ---- pass 2: weighted sum of the value rows
-  float acc[G][E];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
-  for (int p0 = 0; p0 < nrows; p0 += ROWS_PER_PASS * U) {
-    uint4 vv[U][V16];
-    bool act[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + p0 + u * ROWS_PER_PASS + warp * RPW + rg;
-      act[u] = state_ok && r < r1 && mrow[r] != 0;
-      if (act[u]) {
-        const uint16_t* src = (r == cur) ? vn : Vc + (long long)r * D;
-#pragma unroll
-        for (int j = 0; j < V16; ++j) vv[u][j] = ld_stream(src + (j * LPR + li) * 8);
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int idx = nspec;
+      for (int c = nspec; c < nchunks; ++c) {
+        if (!chunk_on[c]) continue;
+        const int s = idx % kStages;
+        if (!wait_bar(bar_empty0 + 8 * s, ((idx / kStages) & 1) ^ 1, abort_flag, &st->error)) break;
+        const uint32_t bytes = uint32_t(min(CH, nrows - c * CH)) * D * 2;
+        mbar_arrive_expect_tx(bar_full0 + 8 * s, 2 * bytes);
+        const long long row = r0 + c * CH;
+        bulk_load(sring + s * kStageBytes, Kc + row * D, bytes, bar_full0 + 8 * s);
+        bulk_load(sring + s * kStageBytes + CHUNK_BYTES, Vc + row * D, bytes, bar_full0 + 8 * s);
+        ++idx;
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (!act[u]) continue;
-      const int r = r0 + p0 + u * ROWS_PER_PASS + warp * RPW + rg;
-      float p[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) p[g] = sc[g * sc_len + (r - r0)];
-#pragma unroll
-      for (int j = 0; j < V16; ++j) {
-        float f[8];
-        bf16x8_to_f32(vv[u][j], f);
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[g][j * 8 + e] = fmaf(p[g], f[e], acc[g][j * 8 + e]);
+    // append the step's row to the cache (the compute warps read it from kn_s / vn_s)
+    if (state_ok && cur >= r0 && cur < r1) {
+      for (int i = lane; i < D / 8; i += 32) {
+        reinterpret_cast<uint4*>(Kc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(kn_s)[i];
+        reinterpret_cast<uint4*>(Vc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(vn_s)[i];
       }
     }
-  }
-  // reduce across the row groups of the warp, then across warps
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < E; ++e)
-#pragma unroll
-      for (int o = LPR; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
-  if (rg == 0) {
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int li = lane % LPR, rg = lane / LPR;
+    float qr[G][E];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int j = 0; j < V16; ++j)
+      for (int j = 0; j < V16; ++j) {
+        float f[8];
+        bf16x8_to_f32(qraw[g][j], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) red[(warp * G + g) * D + (j * LPR + li) * 8 + e] = acc[g][j * 8 + e];
+        for (int e = 0; e < 8; ++e) qr[g][j * 8 + e] = f[e] * a.scale_log2;
+      }
+    float m_run[G], l_run[G], acc[G][E];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m_run[g] = -CUDART_INF_F;
+      l_run[g] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+    }
+    const int cur_i = cur - r0;  // the step's row within the range (may be outside)
+    int idx = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      if (!chunk_on[c]) continue;
+      const int s = oneshot ? c : idx % kStages;
+      if (!oneshot) {
+        const bool ok = __all_sync(0xffffffffu, wait_bar(bar_full0 + 8 * s, (idx / kStages) & 1, abort_flag,
+                                                           &st->error));
+        if (!ok) break;
+      }
+      const uint8_t* Ks = smem + s * kStageBytes;
+      const uint8_t* Vs = Ks + CHUNK_BYTES;
+      float sc[PASSES][G];
+      bool valid[PASSES];
+      float cmax[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) cmax[g] = -CUDART_INF_F;
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        const int rr = warp * RPC + p * RPW + rg;  // row within the chunk
+        const int ri = c * CH + rr;                // row within the range
+        valid[p] = ri < nrows && mask_s[ri] != 0;
+        const uint8_t* krow = (ri == cur_i) ? kn_s : Ks + rr * D * 2;
+        float acc_s[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc_s[g] = 0.f;
+#pragma unroll
+        for (int j = 0; j < V16; ++j) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(krow + (j * LPR + li) * 16);
+          float f[8];
+          bf16x8_to_f32(kv, f);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc_s[g] = fmaf(qr[g][j * 8 + e], f[e], acc_s[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+#pragma unroll
+          for (int o = LPR / 2; o > 0; o >>= 1) acc_s[g] += __shfl_xor_sync(0xffffffffu, acc_s[g], o);
+          sc[p][g] = valid[p] ? acc_s[g] : -CUDART_INF_F;
+          cmax[g] = fmaxf(cmax[g], sc[p][g]);
+        }
+      }
+      // chunk maximum over the warp's rows, then rescale the running state
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1) cmax[g] = fmaxf(cmax[g], __shfl_xor_sync(0xffffffffu, cmax[g], o));
+        const float mn = fmaxf(m_run[g], cmax[g]);
+        if (mn > m_run[g]) {
+          const float alpha = (m_run[g] == -CUDART_INF_F) ? 0.f : exp2f(m_run[g] - mn);
+          l_run[g] *= alpha;
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[g][e] *= alpha;
+          m_run[g] = mn;
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < PASSES; ++p) {
+        if (!valid[p]) continue;
+        const int rr = warp * RPC + p * RPW + rg;
+        const uint8_t* vrow = (c * CH + rr == cur_i) ? vn_s : Vs + rr * D * 2;
+        float w[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          w[g] = exp2f(sc[p][g] - m_run[g]);
+          l_run[g] += w[g];
+        }
+#pragma unroll
+        for (int j = 0; j < V16; ++j) {
+          const uint4 vv = *reinterpret_cast<const uint4*>(vrow + (j * LPR + li) * 16);
+          float f[8];
+          bf16x8_to_f32(vv, f);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[g][j * 8 + e] = fmaf(w[g], f[e], acc[g][j * 8 + e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0 && !oneshot) mbar_arrive(bar_empty0 + 8 * s);
+      ++idx;
+    }
+    // reduce the warp's row groups (every lane of a group holds the same weights)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], o);
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+#pragma unroll
+        for (int o = LPR; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        s_m[warp][g] = m_run[g];
+        s_l[warp][g] = l_run[g];
+      }
+    }
+    // every warp rescales to the CTA maximum and the warps are summed into
+    // kSlots shared-memory slots in a fixed order (round r adds warps
+    // [r * kSlots, (r + 1) * kSlots)); the ring is free once all compute warps
+    // are past their chunk loops
+    constexpr int kSlots = merge_slots(G, D);
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+    float* red = reinterpret_cast<float*>(smem);  // [kSlots][G][D]
+    float scale_w[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, s_m[w][g]);
+      scale_w[g] = (m_run[g] == -CUDART_INF_F) ? 0.f : exp2f(m_run[g] - M);
+    }
+    const int slot = warp % kSlots;
+#pragma unroll 1
+    for (int r = 0; r < kComputeWarps / kSlots; ++r) {
+      if (warp / kSlots == r && rg == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int j = 0; j < V16; ++j)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float* d = &red[(slot * G + g) * D + (j * LPR + li) * 8 + e];
+              const float v = scale_w[g] * acc[g][j * 8 + e];
+              *d = (r == 0) ? v : *d + v;
+            }
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+    }
   }
   __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  if (aborted && tid == kComputeWarps * 32) {
+    // let bulk copies in flight land before shared memory is reused or released
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
 
-  // ---- partial result of this split (warps summed in a fixed order: deterministic)
-  const int nsplit = a.nsplit;
-  const long long head0 = (long long)b * a.q_heads + (long long)h * G;
-  for (int i = tid; i < G * D; i += kDecodeThreads) {
-    const int g = i / D, d = i % D;
-    float sum = red[i];
+  // ---- this CTA's (M, L) and accumulator (slots summed in a fixed order)
+  constexpr int kSlots = merge_slots(G, D);
+  if (tid < G) {
+    float M = -CUDART_INF_F;
+    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, s_m[w][tid]);
+    float L = 0.f;
+    for (int w = 0; w < kComputeWarps; ++w)
+      if (s_m[w][tid] != -CUDART_INF_F) L += exp2f(s_m[w][tid] - M) * s_l[w][tid];
+    s_M[tid] = M;
+    s_L[tid] = L;
+  }
+  float* red = reinterpret_cast<float*>(smem);
+  float* cta_acc = red + kSlots * G * D;  // [G][D]
+  for (int i = tid; i < G * D; i += kThreads) {
+    float o = red[i];
 #pragma unroll
-    for (int w = 1; w < kDecodeWarps; ++w) sum += red[w * G * D + i];
-    a.ws_acc[((head0 + g) * nsplit + split) * D + d] = sum;
+    for (int k = 1; k < kSlots; ++k) o += red[k * G * D + i];
+    cta_acc[i] = o;
+  }
+  __syncthreads();
+  const long long head0 = (long long)b * a.q_heads + (long long)h * G;
+  const int nsplit = a.nsplit;
+
+  if (nsplit == 1) {
+    if (!aborted) {
+      for (int i = tid; i < G * D / 2; i += kThreads) {
+        const int g = (2 * i) / D;
+        const float L = s_L[g];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<uint32_t*>(a.out + head0 * D)[i] = pack_bf16(cta_acc[2 * i] * inv, cta_acc[2 * i + 1] * inv);
+      }
+      if (tid < G && a.lse)
+        a.lse[head0 + tid] = s_L[tid] > 0.f ? (s_M[tid] + log2f(s_L[tid])) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+    return;
+  }
+
+  if (a.cluster) {
+    // ---- cluster merge: rank 0 reads every CTA's (M, L, accumulator) through
+    // distributed shared memory; every CTA reaches both cluster barriers
+    cluster_sync();
+    if (!aborted) {
+      // every CTA merges its own slice of the output columns from all CTAs of
+      // the cluster (remote loads issued together; fixed summation order)
+      float* wts = cta_acc + G * D;  // [G][nsplit]
+      float* sms = wts + G * nsplit;
+      float* sls = sms + G * nsplit;
+      __shared__ float s_gM[G], s_gL[G];
+      for (int x = tid; x < G * nsplit; x += kThreads) {
+        const int g = x / nsplit, r = x % nsplit;
+        sms[x] = ld_dsmem_f32(map_shared(smem_u32(&s_M[g]), r));
+        sls[x] = ld_dsmem_f32(map_shared(smem_u32(&s_L[g]), r));
+      }
+      __syncthreads();
+      if (tid < G) {
+        const int g = tid;
+        float M = -CUDART_INF_F;
+        for (int r = 0; r < nsplit; ++r) M = fmaxf(M, sms[g * nsplit + r]);
+        float L = 0.f;
+        for (int r = 0; r < nsplit; ++r) {
+          const float ms = sms[g * nsplit + r];
+          const float w = (ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
+          wts[g * nsplit + r] = w;
+          L += w * sls[g * nsplit + r];
+        }
+        s_gM[g] = M;
+        s_gL[g] = L;
+      }
+      __syncthreads();
+      const int nf = G * D / 4;
+      const int rank = int(cluster_ctarank());
+      const int f0 = rank * nf / nsplit, f1 = (rank + 1) * nf / nsplit;
+      for (int f = f0 + tid; f < f1; f += kThreads) {
+        const int g = (4 * f) / D;
+        const uint32_t local = smem_u32(cta_acc + 4 * f);
+        float4 v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < nsplit) v[r] = ld_dsmem_f32x4(map_shared(local, r));
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+          if (r < nsplit) {
+            const float w = wts[g * nsplit + r];
+            o.x = fmaf(w, v[r].x, o.x);
+            o.y = fmaf(w, v[r].y, o.y);
+            o.z = fmaf(w, v[r].z, o.z);
+            o.w = fmaf(w, v[r].w, o.w);
+          }
+        const float L = s_gL[g];
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        reinterpret_cast<uint2*>(a.out + head0 * D)[f] =
+            make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+      }
+      if (rank == 0 && tid < G && a.lse)
+        a.lse[head0 + tid] = s_gL[tid] > 0.f ? (s_gM[tid] + log2f(s_gL[tid])) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+    cluster_sync();
+    return;
+  }
+
+  // ---- workspace merge
+  if (aborted) return;
+  for (int i = tid; i < G * D; i += kThreads) {
+    const int g = i / D, d = i % D;
+    a.ws_acc[((head0 + g) * nsplit + split) * D + d] = cta_acc[i];
   }
   if (tid < G) {
-    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 0] = s_m[tid];
-    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 1] = s_l[tid];
+    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 0] = s_M[tid];
+    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 1] = s_L[tid];
   }
   __threadfence();
   __syncthreads();
@@ -275,16 +525,12 @@ decode_kernel(const DecodeArgs a) {
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-
-  // ---- combine (last CTA of this sequence and kv head)
-  // split statistics are staged in shared memory with independent loads; the
-  // accumulator loads are issued eight at a time; the summation order over
-  // splits stays fixed (deterministic)
-  float* wts = red;                     // [G][nsplit] merge weights
-  float* sms = red + G * nsplit;        // [G][nsplit] split maxima
-  float* sls = red + 2 * G * nsplit;    // [G][nsplit] split sums
-  __shared__ float s_M[G], s_L[G];
-  for (int x = tid; x < G * nsplit; x += kDecodeThreads) {
+  // last CTA of the slab: statistics staged with independent loads, then the
+  // accumulators 16 splits at a time as float4 (fixed summation order)
+  float* wts = cta_acc + G * D;  // [G][nsplit]
+  float* sms = wts + G * nsplit;
+  float* sls = sms + G * nsplit;
+  for (int x = tid; x < G * nsplit; x += kThreads) {
     const int g = x / nsplit, s = x % nsplit;
     sms[x] = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2]);
     sls[x] = __ldcg(&a.ws_ml[((head0 + g) * nsplit + s) * 2 + 1]);
@@ -305,43 +551,72 @@ decode_kernel(const DecodeArgs a) {
     s_L[g] = Lsum;
   }
   __syncthreads();
-  for (int i = tid; i < G * D; i += kDecodeThreads) {
-    const int g = i / D, d = i % D;
-    const float* src = a.ws_acc + (head0 + g) * nsplit * (long long)D + d;
-    const float* w = wts + g * nsplit;
-    float o = 0.f;
-    int s = 0;
-    for (; s + 8 <= nsplit; s += 8) {
-      float v[8];
+  for (int f = tid; f < G * D / 4; f += kThreads) {
+    const int g = (4 * f) / D, d = (4 * f) % D;
+    const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (head0 + g) * nsplit * (long long)D + d);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += 16) {
+      float4 v[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (long long)(s + u) * D);
+      for (int u = 0; u < 16; ++u)
+        if (s0 + u < nsplit) v[u] = __ldcg(src + (long long)(s0 + u) * (D / 4));
 #pragma unroll
-      for (int u = 0; u < 8; ++u) o = fmaf(w[s + u], v[u], o);
+      for (int u = 0; u < 16; ++u)
+        if (s0 + u < nsplit) {
+          const float w = wts[g * nsplit + s0 + u];
+          o.x = fmaf(w, v[u].x, o.x);
+          o.y = fmaf(w, v[u].y, o.y);
+          o.z = fmaf(w, v[u].z, o.z);
+          o.w = fmaf(w, v[u].w, o.w);
+        }
     }
-    for (; s < nsplit; ++s) o = fmaf(w[s], __ldcg(src + (long long)s * D), o);
     const float L = s_L[g];
-    o = L > 0.f ? o / L : 0.f;
-    a.out[(head0 + g) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    reinterpret_cast<uint2*>(a.out + head0 * D)[f] =
+        make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
   }
-  if (tid < G && a.lse) {
-    const float L = s_L[tid];
-    a.lse[head0 + tid] = L > 0.f ? (s_M[tid] + log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
-  }
+  if (tid < G && a.lse)
+    a.lse[head0 + tid] = s_L[tid] > 0.f ? (s_M[tid] + log2f(s_L[tid])) * 0.69314718055994530942f : -CUDART_INF_F;
   if (tid == 0) a.counters[b * a.kv_heads + h] = 0;
+}
+
+size_t smem_bytes(int rows_per_split, int ch, int d) {
+  const size_t ring = size_t(kStages) * kStageBytes;
+  const size_t mask = (size_t(rows_per_split) + 15) & ~size_t(15);
+  const size_t flags = ((size_t(rows_per_split) + ch - 1) / ch + 15) & ~size_t(15);
+  return ring + 4 * size_t(d) + mask + flags + 2 * kStages * 8 + 16;
 }
 
 template <int D, int G>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
-  const int sc_len = a.rows_per_split > a.nsplit ? a.rows_per_split : a.nsplit;
-  const size_t smem = sizeof(float) * (size_t(G) * sc_len + size_t(kDecodeWarps) * G * D);
-  auto k = decode_kernel<D, G>;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-    if (e != cudaSuccess) return e;
+  // the merge areas reuse the ring
+  if (size_t(merge_slots(G, D) + 1) * G * D * 4 + size_t(3) * G * a.nsplit * 4 > size_t(kStages) * kStageBytes)
+    return cudaErrorInvalidValue;
+  const size_t smem = smem_bytes(a.rows_per_split, Shape<D, G>::CH, D);
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    if (attr == cudaSuccess)
+      attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  });
+  if (attr != cudaSuccess) return attr;
+  if (smem > 160 * 1024) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.nsplit, a.kv_heads, a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[1];
+  if (a.cluster) {
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = a.nsplit;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
   }
-  dim3 grid(a.nsplit, a.kv_heads, a.batch);
-  k<<<grid, kDecodeThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, a);
 }
 
 template <int D>
@@ -357,19 +632,23 @@ cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count) {
+DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count,
+                         int max_cluster) {
   DecodeSplit d;
+  const int ch = kStageBytes / (2 * head_dim * 2);
   const long long pairs = (long long)batch * kv_heads;
-  const long long target = 4LL * (sm_count > 0 ? sm_count : 152);
+  const long long target = 2LL * (sm_count > 0 ? sm_count : 152);
+  const int min_rows = 2 * ch > 64 ? 2 * ch : 64;
   long long ns = (target + pairs - 1) / pairs;
-  const int min_rows = 32;
   long long max_ns = (rows + min_rows - 1) / min_rows;
   if (max_ns > 64) max_ns = 64;
   if (ns > max_ns) ns = max_ns;
   if (ns < 1) ns = 1;
-  d.nsplit = int(ns);
-  d.rows_per_split = (rows + d.nsplit - 1) / d.nsplit;
+  // prefer one cluster per slab when its splits stay short (<= 8 chunks each)
+  if (ns > max_cluster && (rows + max_cluster - 1) / max_cluster <= 8 * ch) ns = max_cluster;
+  d.rows_per_split = int((rows + ns - 1) / ns);
   d.nsplit = (rows + d.rows_per_split - 1) / d.rows_per_split;
+  d.cluster = (d.nsplit > 1 && d.nsplit <= max_cluster) ? 1 : 0;
   const size_t counters = size_t(pairs) * sizeof(int32_t);
   const size_t ml = size_t(batch) * q_heads * d.nsplit * 2 * sizeof(float);
   const size_t acc = size_t(batch) * q_heads * d.nsplit * head_dim * sizeof(float);
@@ -377,6 +656,39 @@ DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int
   d.off_acc = d.off_ml + align256(ml);
   d.total = d.off_acc + align256(acc);
   return d;
+}
+
+int decode_max_cluster() {
+  // the largest cluster of decode CTAs the current device can co-schedule
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int best = 8;
+    if (cudaFuncSetAttribute(decode_kernel<256, 2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(decode_kernel<256, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+            cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = smem_bytes(128, Shape<256, 2>::CH, 256);
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 16;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<256, 2>, &cfg) == cudaSuccess && n >= 2) best = 16;
+      cudaGetLastError();
+    }
+    cached[dev] = best;
+  }
+  return cached[dev];
 }
 
 cudaError_t decode_static_scratch(void** ptr) {

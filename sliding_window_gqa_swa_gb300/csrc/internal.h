@@ -107,15 +107,19 @@ struct DecodeArgs {
   float* ws_acc;          // [B, Hq, nsplit, D]
   int batch, q_heads, kv_heads, head_dim, rows, layer;
   int nsplit, rows_per_split;
+  int cluster;            // 1: the splits of a slab form one cluster and merge in shared memory
   float scale_log2;       // scale * log2(e)
 };
 
 // Split choice and workspace size shared by the host API and the launcher.
 struct DecodeSplit {
-  int nsplit, rows_per_split;
+  int nsplit, rows_per_split, cluster;
   size_t off_ml, off_acc, total;
 };
-DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count);
+DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count,
+                         int max_cluster);
+// Largest decode cluster the current device co-schedules (16 or 8).
+int decode_max_cluster();
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

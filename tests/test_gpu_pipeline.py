@@ -123,8 +123,11 @@ def test_workload1_prefill_compact_decode(swa):
     assert_lse(dec_l, ref_l, "decode lse")
 
 
+# covers the three ways a decode merges its splits: one split per slab, one
+# cluster per slab, and the workspace merge (many splits of a long window)
 @pytest.mark.parametrize("batch,hq,hkv,d,w,s", [(3, 4, 2, 256, 64, 40), (2, 8, 2, 128, 64, 300),
-                                                (2, 8, 1, 64, 128, 129), (1, 8, 8, 512, 64, 100)])
+                                                (2, 8, 1, 64, 128, 129), (1, 8, 8, 512, 64, 100),
+                                                (1, 2, 1, 256, 4096, 4200), (1, 4, 2, 256, 1024, 1500)])
 def test_decode_shapes_with_padding(swa, batch, hq, hkv, d, w, s):
     c = synth.decode_case(3100 + d + hq, batch=batch, q_heads=hq, kv_heads=hkv, head_dim=d, window=w,
                           prompt_len=s, steps=140, layers=1, with_prompt_q=False)
