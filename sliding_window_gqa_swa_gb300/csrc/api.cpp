@@ -415,7 +415,7 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
     a.key_dim_rows = meta->seq_len;
     a.err = reinterpret_cast<int32_t*>(const_cast<void*>(meta->plan)) + offsetof(swa::PlanHeader, error) / 4;
   }
-  cudaError_t e = head_dim == 256 ? swa::launch_prefill_tc(a, stream) : swa::launch_prefill_simt(a, stream);
+  cudaError_t e = swa::launch_prefill_tc(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   return SWA_OK;
 }

@@ -147,9 +147,7 @@ struct PrefillArgs {
   int32_t* err;                // device error word (cache state or plan header)
 };
 
-// Tensor-core (tcgen05) prefill, head size 256.
+// Tensor-core (tcgen05) prefill: head size 256 in one CTA, 512 in a CTA pair.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
-// CUDA-core prefill (head size 512).
-cudaError_t launch_prefill_simt(const PrefillArgs& a, cudaStream_t s);
 
 }  // namespace swa

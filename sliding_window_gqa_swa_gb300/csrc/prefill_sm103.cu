@@ -1,27 +1,35 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05), head size 256.
+// Prefill attention on the 5th-generation tensor cores (tcgen05): head size
+// 256 in one CTA, head size 512 in a pair of CTAs.
 //
-// One CTA computes 128 query rows of one query head against the key tiles
-// (64 keys each) its rows need -- the tile range comes from the causal
-// arithmetic or from the plan built on the device (generic plan: image
-// blocks, documents).  Warp roles:
-//   warp 0     TMA producer: Q once, then K_j and V_j tiles into a 4-stage
-//              ring of 32 KB slots (128-byte swizzled, 64-column boxes);
-//   warp 1     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//              S buffers (16 MMAs of 128x64x16), then O += P_{j-1} V_{j-1}
-//              (4 MMAs of 128x256x16, V read MN-major) into the TMEM O
-//              accumulator; owns the TMEM allocation;
+// One CTA computes 128 query rows of one query head, over a 256-column slice
+// of the head dimension, against the key tiles (64 keys each) its rows need;
+// the tile range comes from the causal arithmetic or from the plan built on
+// the device (generic plan: image blocks, documents).  Warp roles:
+//   warp 0     TMA producer: its Q slice once, then K_j and V_j slices into
+//              a ring of 32 KB slots (128-byte swizzled, 64-column boxes);
+//   warp 1     MMA issuer (one thread): S_j = Q K_j^T over the slice into one
+//              of two TMEM S buffers (16 MMAs of 128x64x16), then
+//              O += P_{j-1} V_{j-1} (4 MMAs of 128x256x16, V read MN-major)
+//              into the TMEM O accumulator; owns the TMEM allocation;
 //   warps 2-5  softmax, one thread per query row (its TMEM lane): load the
-//              S row, apply the row's key interval [lo, hi], online softmax
-//              in the exp2 domain with lazy rescaling of O (only when the row
+//              S row, apply the row's key interval [lo, hi], online softmax in
+//              the exp2 domain with lazy rescaling of O (only when the row
 //              maximum grows by more than 2^8), write P (bf16) to shared
 //              memory, and finally normalise O and store it.
+// Head size 512: the two CTAs of a cluster hold the two column halves.  Each
+// computes a partial S over its half of the contraction and sends it to its
+// peer through distributed shared memory; both add the two partials
+// (fp32 addition commutes, so both obtain the same S bit for bit), run the
+// identical softmax, and accumulate their own half of O -- no MMA is done
+// twice.
 // Every wait is bounded; a timeout sets the device error word, makes all
 // roles stop, lets in-flight copies and MMAs finish, and frees TMEM.
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
 // variants", Summary and Compilation behavior (causal square-prefill plan,
 // generic plan for future same-image pairs); "Add SDPA attention
-// implementation", Summary (packed documents, K/V shared by query-head groups).
+// implementation", Summary (packed documents, head size 512, K/V shared by
+// query-head groups).
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -40,31 +48,37 @@ using namespace ptx;
 
 constexpr int BM = kPlanBM;  // 128 query rows per CTA
 constexpr int BN = 64;       // keys per tile
-constexpr int HD = 256;      // head size
-constexpr int NST = 4;       // K/V ring stages
+constexpr int HS = 256;      // head-dimension slice per CTA
 constexpr int kThreads = 192;
 constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KB
 constexpr int KV_CHUNK = BN * 128;       // one 64-column box of K or V: 8 KB
-constexpr int Q_BYTES = Q_CHUNK * (HD / 64);
-constexpr int KV_BYTES = KV_CHUNK * (HD / 64);
+constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
+constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + Q_BYTES;
-constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
-constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int N_BARS = 2 * NST + 8;
-constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
+constexpr int XS_BYTES = BM * BN * 4;    // partial-S exchange buffer (pair only)
 
-constexpr uint32_t TM_O = 0, TM_S0 = HD, TM_S1 = HD + BN, TM_COLS = 512;
+template <bool kPair>
+struct Layout {
+  static constexpr int NST = kPair ? 3 : 4;  // K/V ring stages
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
+  static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_XS + (kPair ? XS_BYTES : 0);
+  static constexpr int N_BARS = 2 * NST + 10;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
+  static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+constexpr uint32_t TM_O = 0, TM_S0 = HS, TM_S1 = HS + BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HD, true);
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 static_assert(TM_S1 + BN <= TM_COLS, "TMEM budget");
 
+template <int NST>
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
@@ -74,15 +88,19 @@ struct Bars {
   __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 3 + b); }
   __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 5 + b); }
   __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 7); }
+  __device__ uint32_t xs_full() const { return base + 8 * (2 * NST + 8); }  // peer's partial arrived
+  __device__ uint32_t xs_free() const { return base + 8 * (2 * NST + 9); }  // peer consumed my partial
 };
 
 // Bounded wait on one phase of an mbarrier.  Gives up when another role has
 // aborted or after kTimeoutNs, recording the timeout.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&] { return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((it & 63) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kTimeoutNs) {
@@ -99,21 +117,28 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  using LY = Layout<kPair>;
+  constexpr int NST = LY::NST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + OFF_Q, sKV = base + OFF_KV, sP = base + OFF_P;
-  const Bars bars{base + OFF_BAR};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + OFF_MISC + 4);
+  const uint32_t sQ = base + LY::OFF_Q, sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
+  const Bars<NST> bars{base + LY::OFF_BAR};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + LY::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
   int32_t* err = a.err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hq = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  const int half = kPair ? int(cluster_ctarank()) : 0;  // which column half of the head
+  const int peer = half ^ 1;
+  const int col0 = half * HS;
+  const int hq = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  const int qt = blockIdx.y, b = blockIdx.z;
   const int hk = hq / (a.q_heads / a.kv_heads);
   const int i0 = qt * BM;
   const int q0 = a.chunk_start + i0;
@@ -152,6 +177,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
+    mbar_init(bars.xs_full(), 128);
+    mbar_init(bars.xs_free(), 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -165,7 +192,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     prefetch_tmap(&tm_v);
   }
   tc_fence_before();
-  __syncthreads();
+  if (kPair) {
+    cluster_sync();  // the peer's barriers are initialised before any remote arrive
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -174,7 +205,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (n > 0) {
       if (lane == 0) {
         mbar_arrive_expect_tx(bars.q(), Q_BYTES);
-        for (int c = 0; c < HD / 64; ++c) tma_load_4d(sQ + c * Q_CHUNK, &tm_q, bars.q(), 64 * c, i0, hq, b);
+        for (int c = 0; c < HS / 64; ++c) tma_load_4d(sQ + c * Q_CHUNK, &tm_q, bars.q(), col0 + 64 * c, i0, hq, b);
       }
       __syncwarp();
       bool ok = true;
@@ -186,8 +217,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           if (ok && lane == 0) {
             mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
             const CUtensorMap* m = x ? &tm_v : &tm_k;
-            for (int c = 0; c < HD / 64; ++c)
-              tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), 64 * c, k0, hk, b);
+            for (int c = 0; c < HS / 64; ++c)
+              tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
           }
           __syncwarp();
         }
@@ -209,7 +240,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tc_fence_after();
             const uint32_t d = tmem + (sb ? TM_S1 : TM_S0);
 #pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
+            for (int kk = 0; kk < HS / 16; ++kk) {
               const int c = kk >> 2, sub = kk & 3;
               const uint64_t ad = sdesc_sw128(sQ + c * Q_CHUNK + sub * 32, 16, 1024);
               const uint64_t bd = sdesc_sw128(sKV + s * KV_BYTES + c * KV_CHUNK + sub * 32, 16, 1024);
@@ -263,6 +294,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       hi = min(hi, a.key_rows - 1);
     }
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    // my row of the exchange buffer, and the same row in the peer's buffer
+    const uint32_t xs_row = base + LY::OFF_XS + r * BN * 4;
+    const uint32_t xs_row_peer = kPair ? map_shared(xs_row, peer) : 0;
+    const uint32_t xs_full_peer = kPair ? map_shared(bars.xs_full(), peer) : 0;
+    const uint32_t xs_free_peer = kPair ? map_shared(bars.xs_free(), peer) : 0;
     // l_run sums the bf16-rounded probabilities (normalises O, which the
     // tensor core accumulates from the same rounded values); l_exact sums the
     // unrounded ones (gives the lse)
@@ -278,6 +314,31 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tmem_ld32(sAddr, sr);
       tmem_ld32(sAddr + 32, sr + 32);
       tmem_ld_wait();
+      if (kPair) {
+        // send my partial row to the peer (once it has consumed the previous
+        // one), then add the peer's partial row to mine
+        if (t > 0) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(), (t - 1) & 1, abort_flag, err));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c = 0; c < BN; c += 4)
+          st_dsmem_f32x4(xs_row_peer + c * 4, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]),
+                         __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+        mbar_arrive_remote(xs_full_peer);
+        ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_full(), t & 1, abort_flag, err));
+        if (!ok) break;
+        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS + r * BN * 4);
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(xr + c);
+          sr[c] = __float_as_uint(__uint_as_float(sr[c]) + v.x);
+          sr[c + 1] = __float_as_uint(__uint_as_float(sr[c + 1]) + v.y);
+          sr[c + 2] = __float_as_uint(__uint_as_float(sr[c + 2]) + v.z);
+          sr[c + 3] = __float_as_uint(__uint_as_float(sr[c + 3]) + v.w);
+        }
+        mbar_arrive_remote(xs_free_peer);
+      }
       const int k0 = (kt_lo + t) * BN;
       const bool full = (k0 >= lo) && (k0 + BN - 1 <= hi);
       float mt = -CUDART_INF_F;
@@ -296,7 +357,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (!ok) break;
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
-        for (int c0 = 0; c0 < HD; c0 += 32) {
+        for (int c0 = 0; c0 < HS; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + TM_O + c0, o);
           tmem_ld_wait();
@@ -332,7 +393,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
         if (!ok) break;
       }
-      uint8_t* prow = gbase + OFF_P + pb * P_BYTES + r * 128;
+      uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
@@ -341,14 +402,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       tc_fence_before();
       mbar_arrive(bars.p_full(pb));
     }
-    // epilogue: O / l -> bf16
+    // epilogue: O / l -> bf16, this CTA's column slice
     bool have_o = n > 0 && ok;
     if (have_o)
       have_o = __all_sync(0xffffffffu, wait_bar(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
     tc_fence_after();
     const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-    uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * HD;
-    for (int c0 = 0; c0 < HD; c0 += 32) {
+    uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0;
+    for (int c0 = 0; c0 < HS; c0 += 32) {
       uint32_t o[32];
       if (have_o) {
         tmem_ld32(tmem + lane_off + TM_O + c0, o);
@@ -364,7 +425,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
       }
     }
-    if (row_ok && a.lse)
+    if (row_ok && a.lse && half == 0)
       a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] =
           l_exact > 0.f ? (m_run + log2f(l_exact)) * 0.69314718055994530942f : -CUDART_INF_F;
   }
@@ -388,6 +449,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncthreads();
   }
+  if (kPair) cluster_sync();  // the peer no longer writes into this CTA's shared memory
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, TM_COLS);
 }
@@ -419,9 +481,38 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   return r == CUDA_SUCCESS;
 }
 
+template <bool kPair>
+cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
+                        cudaStream_t s) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout<kPair>::SMEM);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int nqt = (a.chunk_len + BM - 1) / BM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.q_heads * (kPair ? 2 : 1), nqt, a.batch);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<kPair>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  if (kPair) {
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair>, mq, mk, mv, a);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
+  if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   const uint64_t D = uint64_t(a.head_dim);
   CUtensorMap mq, mk, mv;
   // Q / out [B, C, Hq, D]: dims {D, C, Hq, B}
@@ -433,16 +524,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
   if (!make_map(&mq, a.q, qd, qs, BM) || !make_map(&mk, a.k, kd, ks, BN) || !make_map(&mv, a.v, kd, ks, BN))
     return cudaErrorInvalidValue;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  const int nqt = (a.chunk_len + BM - 1) / BM;
-  dim3 grid(a.q_heads, nqt, a.batch);
-  prefill_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(mq, mk, mv, a);
-  return cudaGetLastError();
+  return a.head_dim == 256 ? launch_kind<false>(mq, mk, mv, a, s) : launch_kind<true>(mq, mk, mv, a, s);
 }
 
 }  // namespace swa
