@@ -496,6 +496,7 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   a.nsplit = sp.nsplit;
   a.rows_per_split = sp.rows_per_split;
   a.cluster = sp.cluster;
+  a.warps = sp.warps;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -555,6 +556,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   a.nsplit = sp.nsplit;
   a.rows_per_split = sp.rows_per_split;
   a.cluster = sp.cluster;
+  a.warps = sp.warps;
   a.scale_log2 = scale * 1.4426950408889634f;
   e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");

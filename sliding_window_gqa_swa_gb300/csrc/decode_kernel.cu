@@ -45,20 +45,19 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kComputeWarps = 16;
-constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
 constexpr int kStages = 3;
 constexpr int kStageBytes = 32768;                  // K chunk + V chunk
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
-template <int D, int G>
+template <int D, int G, int NW>
 struct Shape {
   static constexpr int CH = kStageBytes / (2 * D * 2);  // rows per chunk
-  static constexpr int RPC = CH / kComputeWarps;        // rows per warp per chunk
-  static constexpr int kWant = D * G / 64;              // lanes per row keeping q + acc in registers
+  static constexpr int RPC = CH / NW;                   // rows per warp per chunk
+  static constexpr int kWant = D * G / 32;              // lanes per row keeping q + acc in registers
   static constexpr int kMin = 32 / RPC;                 // a warp pass must not exceed its rows
   static constexpr int kLpr = kWant > kMin ? kWant : kMin;
-  static constexpr int LPR = kLpr < 8 ? 8 : (kLpr > 32 ? 32 : kLpr);  // lanes per row
+  static constexpr int kMax = D / 8 < 32 ? D / 8 : 32;  // a lane holds at least one 16-byte vector
+  static constexpr int LPR = kLpr < 8 ? 8 : (kLpr > kMax ? kMax : kLpr);  // lanes per row
   static constexpr int E = D / LPR;                     // elements per lane
   static constexpr int V16 = E / 8;                     // 16-byte vectors per lane per row
   static constexpr int RPW = 32 / LPR;                  // rows per warp pass
@@ -69,13 +68,27 @@ struct Shape {
 // Shared-memory slots the warp merge uses: as many as fit in the ring next
 // to the CTA accumulator and the combine's statistics (a power of two that
 // divides the warp count).
-__host__ __device__ constexpr int merge_slots(int g, int d) {
-  return (kComputeWarps + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps
-         : (kComputeWarps / 2 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 2
-         : (kComputeWarps / 4 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 4
-         : (kComputeWarps / 8 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? kComputeWarps / 8
-                                                                                        : 1;
+__host__ __device__ constexpr int merge_slots(int nw, int g, int d) {
+  return (nw + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes       ? nw
+         : (nw / 2 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? nw / 2
+         : (nw / 4 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? nw / 4
+         : (nw / 8 + 2) * g * d * 4 + 3 * g * 64 * 4 <= kStages * kStageBytes ? nw / 8
+                                                                               : 1;
 }
+
+// Packed fp32 pairs: (lo, hi) in one 64-bit register and d += a * b on both.
+__device__ __forceinline__ uint64_t pair_f32(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+__device__ __forceinline__ void ffma2(uint64_t& d, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ float pair_lo(uint64_t x) { return __uint_as_float(uint32_t(x)); }
+__device__ __forceinline__ float pair_hi(uint64_t x) { return __uint_as_float(uint32_t(x >> 32)); }
+// bf16 pair (element 0 in the low half) widened to an fp32 pair
+__device__ __forceinline__ uint64_t bf16x2_to_pair(uint32_t w) { return pair_f32(w << 16, w & 0xffff0000u); }
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -111,10 +124,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // chunk loop for the per-warp accumulators [warps][G][D], the CTA accumulator
 // [G][D] and the combine's split statistics) | new K row | new V row | mask
 // bytes of the range | chunk flags | barriers.
-template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int G, int NW>
+__global__ void __launch_bounds__(32 * (NW + 1), 16 / NW)
 decode_kernel(const DecodeArgs a) {
-  using S = Shape<D, G>;
+  constexpr int kComputeWarps = NW;
+  constexpr int kThreads = 32 * (NW + 1);  // + one producer warp
+  using S = Shape<D, G, NW>;
   constexpr int LPR = S::LPR, E = S::E, V16 = S::V16, RPW = S::RPW, CH = S::CH, RPC = S::RPC,
                 PASSES = S::PASSES;
   constexpr int CHUNK_BYTES = CH * D * 2;
@@ -244,7 +259,8 @@ decode_kernel(const DecodeArgs a) {
   } else {
     // ------------------------------------------------------------ compute warps
     const int li = lane % LPR, rg = lane / LPR;
-    float qr[G][E];
+    // query slice as fp32 pairs, pre-scaled into the exp2 domain
+    uint64_t qr[G][E / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -252,15 +268,17 @@ decode_kernel(const DecodeArgs a) {
         float f[8];
         bf16x8_to_f32(qraw[g][j], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) qr[g][j * 8 + e] = f[e] * a.scale_log2;
+        for (int e = 0; e < 8; e += 2)
+          qr[g][(j * 8 + e) / 2] = pair_f32(__float_as_uint(f[e] * a.scale_log2), __float_as_uint(f[e + 1] * a.scale_log2));
       }
-    float m_run[G], l_run[G], acc[G][E];
+    float m_run[G], l_run[G];
+    uint64_t acc[G][E / 2];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       m_run[g] = -CUDART_INF_F;
       l_run[g] = 0.f;
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
+      for (int e = 0; e < E / 2; ++e) acc[g][e] = 0ull;
     }
     const int cur_i = cur - r0;  // the step's row within the range (may be outside)
     int idx = 0;
@@ -285,21 +303,24 @@ decode_kernel(const DecodeArgs a) {
         const int ri = c * CH + rr;                // row within the range
         valid[p] = ri < nrows && mask_s[ri] != 0;
         const uint8_t* krow = (ri == cur_i) ? kn_s : Ks + rr * D * 2;
-        float acc_s[G];
+        uint64_t acc2[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) acc_s[g] = 0.f;
+        for (int g = 0; g < G; ++g) acc2[g] = 0ull;
 #pragma unroll
         for (int j = 0; j < V16; ++j) {
           const uint4 kv = *reinterpret_cast<const uint4*>(krow + (j * LPR + li) * 16);
-          float f[8];
-          bf16x8_to_f32(kv, f);
+          const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
-          for (int g = 0; g < G; ++g)
+          for (int e = 0; e < 4; ++e) {
+            const uint64_t k2 = bf16x2_to_pair(w[e]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc_s[g] = fmaf(qr[g][j * 8 + e], f[e], acc_s[g]);
+            for (int g = 0; g < G; ++g) ffma2(acc2[g], qr[g][j * 4 + e], k2);
+          }
         }
+        float acc_s[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
+          acc_s[g] = pair_lo(acc2[g]) + pair_hi(acc2[g]);
 #pragma unroll
           for (int o = LPR / 2; o > 0; o >>= 1) acc_s[g] += __shfl_xor_sync(0xffffffffu, acc_s[g], o);
           sc[p][g] = valid[p] ? acc_s[g] : -CUDART_INF_F;
@@ -315,8 +336,13 @@ decode_kernel(const DecodeArgs a) {
         if (mn > m_run[g]) {
           const float alpha = (m_run[g] == -CUDART_INF_F) ? 0.f : exp2f(m_run[g] - mn);
           l_run[g] *= alpha;
+          const uint64_t a2 = pair_f32(__float_as_uint(alpha), __float_as_uint(alpha));
 #pragma unroll
-          for (int e = 0; e < E; ++e) acc[g][e] *= alpha;
+          for (int e = 0; e < E / 2; ++e) {
+            uint64_t z = 0ull;
+            ffma2(z, acc[g][e], a2);
+            acc[g][e] = z;
+          }
           m_run[g] = mn;
         }
       }
@@ -325,21 +351,23 @@ decode_kernel(const DecodeArgs a) {
         if (!valid[p]) continue;
         const int rr = warp * RPC + p * RPW + rg;
         const uint8_t* vrow = (c * CH + rr == cur_i) ? vn_s : Vs + rr * D * 2;
-        float w[G];
+        uint64_t w2[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          w[g] = exp2f(sc[p][g] - m_run[g]);
-          l_run[g] += w[g];
+          const float w = exp2f(sc[p][g] - m_run[g]);
+          l_run[g] += w;
+          w2[g] = pair_f32(__float_as_uint(w), __float_as_uint(w));
         }
 #pragma unroll
         for (int j = 0; j < V16; ++j) {
           const uint4 vv = *reinterpret_cast<const uint4*>(vrow + (j * LPR + li) * 16);
-          float f[8];
-          bf16x8_to_f32(vv, f);
+          const uint32_t wv[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-          for (int g = 0; g < G; ++g)
+          for (int e = 0; e < 4; ++e) {
+            const uint64_t v2 = bf16x2_to_pair(wv[e]);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[g][j * 8 + e] = fmaf(w[g], f[e], acc[g][j * 8 + e]);
+            for (int g = 0; g < G; ++g) ffma2(acc[g][j * 4 + e], w2[g], v2);
+          }
         }
       }
       __syncwarp();
@@ -352,9 +380,15 @@ decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int o = LPR; o < 32; o <<= 1) l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], o);
 #pragma unroll
-      for (int e = 0; e < E; ++e)
+      for (int e = 0; e < E / 2; ++e) {
+        float lo = pair_lo(acc[g][e]), hi = pair_hi(acc[g][e]);
 #pragma unroll
-        for (int o = LPR; o < 32; o <<= 1) acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], o);
+        for (int o = LPR; o < 32; o <<= 1) {
+          lo += __shfl_xor_sync(0xffffffffu, lo, o);
+          hi += __shfl_xor_sync(0xffffffffu, hi, o);
+        }
+        acc[g][e] = pair_f32(__float_as_uint(lo), __float_as_uint(hi));
+      }
     }
     if (lane == 0) {
 #pragma unroll
@@ -367,7 +401,7 @@ decode_kernel(const DecodeArgs a) {
     // kSlots shared-memory slots in a fixed order (round r adds warps
     // [r * kSlots, (r + 1) * kSlots)); the ring is free once all compute warps
     // are past their chunk loops
-    constexpr int kSlots = merge_slots(G, D);
+    constexpr int kSlots = merge_slots(NW, G, D);
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
     float* red = reinterpret_cast<float*>(smem);  // [kSlots][G][D]
     float scale_w[G];
@@ -389,7 +423,8 @@ decode_kernel(const DecodeArgs a) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               float* d = &red[(slot * G + g) * D + (j * LPR + li) * 8 + e];
-              const float v = scale_w[g] * acc[g][j * 8 + e];
+              const uint64_t pr = acc[g][(j * 8 + e) / 2];
+              const float v = scale_w[g] * ((e & 1) ? pair_hi(pr) : pair_lo(pr));
               *d = (r == 0) ? v : *d + v;
             }
       }
@@ -406,7 +441,7 @@ decode_kernel(const DecodeArgs a) {
   }
 
   // ---- this CTA's (M, L) and accumulator (slots summed in a fixed order)
-  constexpr int kSlots = merge_slots(G, D);
+  constexpr int kSlots = merge_slots(NW, G, D);
   if (tid < G) {
     float M = -CUDART_INF_F;
     for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, s_m[w][tid]);
@@ -587,24 +622,24 @@ size_t smem_bytes(int rows_per_split, int ch, int d) {
   return ring + 4 * size_t(d) + mask + flags + 2 * kStages * 8 + 16;
 }
 
-template <int D, int G>
+template <int D, int G, int NW>
 cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   // the merge areas reuse the ring
-  if (size_t(merge_slots(G, D) + 1) * G * D * 4 + size_t(3) * G * a.nsplit * 4 > size_t(kStages) * kStageBytes)
+  if (size_t(merge_slots(NW, G, D) + 1) * G * D * 4 + size_t(3) * G * a.nsplit * 4 > size_t(kStages) * kStageBytes)
     return cudaErrorInvalidValue;
-  const size_t smem = smem_bytes(a.rows_per_split, Shape<D, G>::CH, D);
+  const size_t smem = smem_bytes(a.rows_per_split, Shape<D, G, NW>::CH, D);
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+    attr = cudaFuncSetAttribute(decode_kernel<D, G, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, 110 * 1024);
     if (attr == cudaSuccess)
-      attr = cudaFuncSetAttribute(decode_kernel<D, G>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      attr = cudaFuncSetAttribute(decode_kernel<D, G, NW>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   });
   if (attr != cudaSuccess) return attr;
-  if (smem > 160 * 1024) return cudaErrorInvalidValue;
+  if (smem > 110 * 1024) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.kv_heads, a.batch);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(32 * (NW + 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attrs[1];
@@ -616,16 +651,21 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, NW>, a);
+}
+
+template <int D, int G>
+cudaError_t launch_w(const DecodeArgs& a, cudaStream_t s) {
+  return a.warps == 16 ? launch_t<D, G, 16>(a, s) : launch_t<D, G, 8>(a, s);
 }
 
 template <int D>
 cudaError_t launch_d(const DecodeArgs& a, cudaStream_t s) {
   switch (a.q_heads / a.kv_heads) {
-    case 1: return launch_t<D, 1>(a, s);
-    case 2: return launch_t<D, 2>(a, s);
-    case 4: return launch_t<D, 4>(a, s);
-    case 8: return launch_t<D, 8>(a, s);
+    case 1: return launch_w<D, 1>(a, s);
+    case 2: return launch_w<D, 2>(a, s);
+    case 4: return launch_w<D, 4>(a, s);
+    case 8: return launch_w<D, 8>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -637,18 +677,28 @@ DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int
   DecodeSplit d;
   const int ch = kStageBytes / (2 * head_dim * 2);
   const long long pairs = (long long)batch * kv_heads;
-  const long long target = 2LL * (sm_count > 0 ? sm_count : 152);
+  const int sms = sm_count > 0 ? sm_count : 152;
   const int min_rows = 2 * ch > 64 ? 2 * ch : 64;
-  long long ns = (target + pairs - 1) / pairs;
   long long max_ns = (rows + min_rows - 1) / min_rows;
   if (max_ns > 64) max_ns = 64;
+  long long ns;
+  if (pairs >= sms) {
+    // throughput regime: 8 compute warps, two CTAs per SM, a few splits per
+    // slab for load balance, merged through the workspace
+    d.warps = 8;
+    ns = (8LL * sms + pairs - 1) / pairs;
+    if (ns > 4) ns = 4;
+  } else {
+    // latency regime: 16 compute warps, as many CTAs as the cluster allows
+    d.warps = 16;
+    ns = (2LL * sms + pairs - 1) / pairs;
+    if (ns > max_cluster && (rows + max_cluster - 1) / max_cluster <= 8 * ch) ns = max_cluster;
+  }
   if (ns > max_ns) ns = max_ns;
   if (ns < 1) ns = 1;
-  // prefer one cluster per slab when its splits stay short (<= 8 chunks each)
-  if (ns > max_cluster && (rows + max_cluster - 1) / max_cluster <= 8 * ch) ns = max_cluster;
   d.rows_per_split = int((rows + ns - 1) / ns);
   d.nsplit = (rows + d.rows_per_split - 1) / d.rows_per_split;
-  d.cluster = (d.nsplit > 1 && d.nsplit <= max_cluster) ? 1 : 0;
+  d.cluster = (d.warps == 16 && d.nsplit > 1 && d.nsplit <= max_cluster) ? 1 : 0;
   const size_t counters = size_t(pairs) * sizeof(int32_t);
   const size_t ml = size_t(batch) * q_heads * d.nsplit * 2 * sizeof(float);
   const size_t acc = size_t(batch) * q_heads * d.nsplit * head_dim * sizeof(float);
@@ -667,14 +717,14 @@ int decode_max_cluster() {
   std::lock_guard<std::mutex> lock(mu);
   if (cached[dev] == 0) {
     int best = 8;
-    if (cudaFuncSetAttribute(decode_kernel<256, 2>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+    if (cudaFuncSetAttribute(decode_kernel<256, 2, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
             cudaSuccess &&
-        cudaFuncSetAttribute(decode_kernel<256, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) ==
+        cudaFuncSetAttribute(decode_kernel<256, 2, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, 110 * 1024) ==
             cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16, 1, 1);
-      cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = smem_bytes(128, Shape<256, 2>::CH, 256);
+      cfg.blockDim = dim3(32 * 17);
+      cfg.dynamicSmemBytes = smem_bytes(128, Shape<256, 2, 16>::CH, 256);
       cudaLaunchAttribute at;
       at.id = cudaLaunchAttributeClusterDimension;
       at.val.clusterDim.x = 16;
@@ -683,7 +733,7 @@ int decode_max_cluster() {
       cfg.attrs = &at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<256, 2>, &cfg) == cudaSuccess && n >= 2) best = 16;
+      if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<256, 2, 16>, &cfg) == cudaSuccess && n >= 2) best = 16;
       cudaGetLastError();
     }
     cached[dev] = best;

@@ -108,12 +108,13 @@ struct DecodeArgs {
   int batch, q_heads, kv_heads, head_dim, rows, layer;
   int nsplit, rows_per_split;
   int cluster;            // 1: the splits of a slab form one cluster and merge in shared memory
+  int warps;              // compute warps per CTA: 8 (throughput) or 16 (latency)
   float scale_log2;       // scale * log2(e)
 };
 
 // Split choice and workspace size shared by the host API and the launcher.
 struct DecodeSplit {
-  int nsplit, rows_per_split, cluster;
+  int nsplit, rows_per_split, cluster, warps;
   size_t off_ml, off_acc, total;
 };
 DecodeSplit decode_split(int batch, int q_heads, int kv_heads, int head_dim, int rows, int sm_count,
