@@ -49,7 +49,7 @@ using namespace ptx;
 constexpr int BM = kPlanBM;  // 128 query rows per CTA
 constexpr int BN = 64;       // keys per tile
 constexpr int HS = 256;      // head-dimension slice per CTA
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
 constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KB
 constexpr int KV_CHUNK = BN * 128;       // one 64-column box of K or V: 8 KB
 constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
@@ -64,7 +64,8 @@ struct Layout {
   static constexpr int OFF_KV = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
   static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_BAR = OFF_XS + (kPair ? XS_BYTES : 0);
+  static constexpr int OFF_PMAX = OFF_XS + (kPair ? XS_BYTES : 0);  // [2 groups][128 rows] fp32
+  static constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
   static constexpr int N_BARS = 2 * NST + 10;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
@@ -173,12 +174,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     mbar_init(bars.q(), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full(i), 1);
-      mbar_init(bars.p_full(i), 128);
+      mbar_init(bars.p_full(i), 256);
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
-    mbar_init(bars.xs_full(), 128);
-    mbar_init(bars.xs_free(), 128);
+    mbar_init(bars.xs_full(), 256);
+    mbar_init(bars.xs_free(), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -275,7 +276,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax (one row per thread)
+    // ------------------------------------------------------------ softmax
+    // Two warpgroups; warp w serves TMEM lane quadrant (w % 4), i.e. one query
+    // row per thread, and group g = 0 / 1 handles score columns [32g, 32g + 32)
+    // of each key tile and output columns [128g, 128g + 128) of the slice.  The
+    // two threads of a row (warps w and w + 4) exchange their tile maxima
+    // through shared memory under a 64-thread named barrier per quadrant, so
+    // both take identical rescaling decisions.
+    const int grp = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int i = i0 + r;
@@ -293,15 +301,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       hi = min(hi, a.key_rows - 1);
     }
+    constexpr int HC = BN / 2;   // score columns per group
+    constexpr int OC = HS / 2;   // output columns per group
+    const int cb = grp * HC;     // first score column of this group
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    // my row of the exchange buffer, and the same row in the peer's buffer
-    const uint32_t xs_row = base + LY::OFF_XS + r * BN * 4;
+    float* pmax = reinterpret_cast<float*>(gbase + LY::OFF_PMAX);  // [group][row]
+    const int bar_id = 1 + q4;   // named barrier of this quadrant's two warps
+    // my row slice of the exchange buffer, and the same slice in the peer's buffer
+    const uint32_t xs_row = base + LY::OFF_XS + (r * BN + cb) * 4;
     const uint32_t xs_row_peer = kPair ? map_shared(xs_row, peer) : 0;
     const uint32_t xs_full_peer = kPair ? map_shared(bars.xs_full(), peer) : 0;
     const uint32_t xs_free_peer = kPair ? map_shared(bars.xs_free(), peer) : 0;
-    // l_run sums the bf16-rounded probabilities (normalises O, which the
-    // tensor core accumulates from the same rounded values); l_exact sums the
-    // unrounded ones (gives the lse)
+    const float c2 = a.scale_log2;
+    // m_run is the reference maximum in the exp2 domain; l_run sums the
+    // bf16-rounded probabilities of this group's columns (normalises O, which
+    // the tensor core accumulates from the same rounded values); l_exact sums
+    // the unrounded ones (gives the lse)
     float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
@@ -309,28 +324,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = __all_sync(0xffffffffu, wait_bar(bars.s_full(sb), (t >> 1) & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[BN];
-      const uint32_t sAddr = tmem + lane_off + (sb ? TM_S1 : TM_S0);
-      tmem_ld32(sAddr, sr);
-      tmem_ld32(sAddr + 32, sr + 32);
+      uint32_t sr[HC];
+      tmem_ld32(tmem + lane_off + (sb ? TM_S1 : TM_S0) + cb, sr);
       tmem_ld_wait();
       if (kPair) {
-        // send my partial row to the peer (once it has consumed the previous
-        // one), then add the peer's partial row to mine
+        // send my partial slice to the peer (once it has consumed the previous
+        // one), then add the peer's partial slice to mine
         if (t > 0) {
           ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(), (t - 1) & 1, abort_flag, err));
           if (!ok) break;
         }
 #pragma unroll
-        for (int c = 0; c < BN; c += 4)
+        for (int c = 0; c < HC; c += 4)
           st_dsmem_f32x4(xs_row_peer + c * 4, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]),
                          __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
         mbar_arrive_remote(xs_full_peer);
         ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_full(), t & 1, abort_flag, err));
         if (!ok) break;
-        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS + r * BN * 4);
+        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS) + r * BN + cb;
 #pragma unroll
-        for (int c = 0; c < BN; c += 4) {
+        for (int c = 0; c < HC; c += 4) {
           const float4 v = *reinterpret_cast<const float4*>(xr + c);
           sr[c] = __float_as_uint(__uint_as_float(sr[c]) + v.x);
           sr[c + 1] = __float_as_uint(__uint_as_float(sr[c + 1]) + v.y);
@@ -339,16 +352,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         mbar_arrive_remote(xs_free_peer);
       }
-      const int k0 = (kt_lo + t) * BN;
-      const bool full = (k0 >= lo) && (k0 + BN - 1 <= hi);
-      float mt = -CUDART_INF_F;
+      // row interval: scores outside [lo, hi] become -inf (raw domain; scale > 0)
+      const int k0 = (kt_lo + t) * BN + cb;
+      const bool full = (k0 >= lo) && (k0 + HC - 1 <= hi);
+      float mraw = -CUDART_INF_F;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        float x = __uint_as_float(sr[c]) * a.scale_log2;
+      for (int c = 0; c < HC; ++c) {
+        float x = __uint_as_float(sr[c]);
         if (!full && (k0 + c < lo || k0 + c > hi)) x = -CUDART_INF_F;
         sr[c] = __float_as_uint(x);
-        mt = fmaxf(mt, x);
+        mraw = fmaxf(mraw, x);
       }
+      // the two groups of this row agree on the tile maximum
+      pmax[grp * BM + r] = mraw;
+      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+      mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
+      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+      const float mt = mraw * c2;
       // lazy rescale: move the reference only when the maximum grows by > 2^8
       const bool move = (m_run == -CUDART_INF_F) ? (mt > -CUDART_INF_F) : (mt > m_run + kRescaleLog2);
       const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
@@ -357,7 +377,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (!ok) break;
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
-        for (int c0 = 0; c0 < HS; c0 += 32) {
+        for (int c0 = grp * OC; c0 < grp * OC + OC; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + TM_O + c0, o);
           tmem_ld_wait();
@@ -372,16 +392,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
       }
       if (move) m_run = mt;
-      // probabilities relative to m_run, packed to bf16; the row sum adds the
-      // same rounded values the PV product uses, so the output is an exact
-      // convex combination of the admitted value rows
-      uint32_t pk[BN / 2];
+      // probabilities exp2(s * scale_log2 - m_run), packed to bf16
+      const float nm = (m_run == -CUDART_INF_F) ? 0.f : -m_run;
+      uint32_t pk[HC / 2];
       float lsum = 0.f, esum = 0.f;
 #pragma unroll
-      for (int c = 0; c < BN; c += 2) {
+      for (int c = 0; c < HC; c += 2) {
         const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
-        const float p0 = (x0 == -CUDART_INF_F) ? 0.f : exp2f(x0 - m_run);
-        const float p1 = (x1 == -CUDART_INF_F) ? 0.f : exp2f(x1 - m_run);
+        const float p0 = exp2f(fmaf(x0, c2, nm));  // -inf -> 0
+        const float p1 = exp2f(fmaf(x1, c2, nm));
         const uint32_t w = pack_bf16(p0, p1);
         lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
         esum += p0 + p1;
@@ -395,21 +414,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<uint4*>(prow + ((j ^ (r & 7)) << 4)) =
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(prow + (((grp * 4 + j) ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bars.p_full(pb));
     }
-    // epilogue: O / l -> bf16, this CTA's column slice
+    // row sums of both groups
+    pmax[grp * BM + r] = l_run;
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    const float l_tot = l_run + pmax[(grp ^ 1) * BM + r];
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    pmax[grp * BM + r] = l_exact;
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    const float e_tot = l_exact + pmax[(grp ^ 1) * BM + r];
+    // epilogue: O / l -> bf16, this group's columns of the CTA's slice
     bool have_o = n > 0 && ok;
     if (have_o)
       have_o = __all_sync(0xffffffffu, wait_bar(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
     tc_fence_after();
-    const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0;
-    for (int c0 = 0; c0 < HS; c0 += 32) {
+    for (int c0 = grp * OC; c0 < grp * OC + OC; c0 += 32) {
       uint32_t o[32];
       if (have_o) {
         tmem_ld32(tmem + lane_off + TM_O + c0, o);
@@ -425,9 +452,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
       }
     }
-    if (row_ok && a.lse && half == 0)
+    if (row_ok && a.lse && half == 0 && grp == 0)
       a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] =
-          l_exact > 0.f ? (m_run + log2f(l_exact)) * 0.69314718055994530942f : -CUDART_INF_F;
+          e_tot > 0.f ? (m_run + log2f(e_tot)) * 0.69314718055994530942f : -CUDART_INF_F;
   }
 
   // ------------------------------------------------------------ teardown
