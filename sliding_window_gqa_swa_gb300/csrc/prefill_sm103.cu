@@ -4,18 +4,29 @@
 // One CTA computes 128 query rows of one query head, over a 256-column slice
 // of the head dimension, against the key tiles (64 keys each) its rows need;
 // the tile range comes from the causal arithmetic or from the plan built on
-// the device (generic plan: image blocks, documents).  Warp roles:
-//   warp 0     TMA producer: its Q slice once, then K_j and V_j slices into
-//              a ring of 32 KB slots (128-byte swizzled, 64-column boxes);
-//   warp 1     MMA issuer (one thread): S_j = Q K_j^T over the slice into one
-//              of two TMEM S buffers (16 MMAs of 128x64x16), then
-//              O += P_{j-1} V_{j-1} (4 MMAs of 128x256x16, V read MN-major)
-//              into the TMEM O accumulator; owns the TMEM allocation;
-//   warps 2-5  softmax, one thread per query row (its TMEM lane): load the
-//              S row, apply the row's key interval [lo, hi], online softmax in
-//              the exp2 domain with lazy rescaling of O (only when the row
-//              maximum grows by more than 2^8), write P (bf16) to shared
-//              memory, and finally normalise O and store it.
+// the device (generic plan: image blocks, documents).
+//
+// Tensor memory (512 columns): O (256 columns, fp32), two S buffers (64
+// columns each) and the CTA's Q slice (128 columns, bf16 pairs), so the
+// score MMAs read only K from shared memory.  Warp roles:
+//   warp 0     TMA producer: K_j and V_j slices into a ring of 32 KB slots
+//              (128-byte swizzled, 64-column boxes), in the order the MMA
+//              warp consumes them: K_0, K_1, then V_j, K_{j+2} for each j;
+//   warp 1     MMA issuer (one thread): S_0 and S_1, then for each tile j one
+//              group that interleaves O += P_j V_j (4 MMAs of 128x256x16, V
+//              read MN-major, P from shared memory) with S_{j+2} = Q K_{j+2}^T
+//              (16 MMAs of 128x64x16, Q from tensor memory) into the S buffer
+//              P_j's scores came from.  The tensor pipe runs consecutive MMAs
+//              of one accumulator back to back only when the MMA is wide;
+//              interleaving the two independent chains keeps it busy;
+//   warps 2-9  softmax: two warpgroups, one query row per thread (its TMEM
+//              lane); group g owns score columns [32g, 32g + 32) of each tile
+//              and output columns [128g, 128g + 128).  Each thread first
+//              copies its share of the Q row into tensor memory.  Per tile:
+//              apply the row's key interval [lo, hi], take the row maximum,
+//              online softmax in the exp2 domain with lazy rescaling of O
+//              (only when the maximum grows by more than 2^8), write P (bf16)
+//              to shared memory; finally normalise O and store it.
 // Head size 512: the two CTAs of a cluster hold the two column halves.  Each
 // computes a partial S over its half of the contraction and sends it to its
 // peer through distributed shared memory; both add the two partials
@@ -46,22 +57,19 @@ namespace {
 
 using namespace ptx;
 
-constexpr int BM = kPlanBM;  // 128 query rows per CTA
-constexpr int BN = 64;       // keys per tile
-constexpr int HS = 256;      // head-dimension slice per CTA
+constexpr int BM = kPlanBM;    // 128 query rows per CTA
+constexpr int BN = 64;         // keys per tile
+constexpr int HS = 256;        // head-dimension slice per CTA
 constexpr int kThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
-constexpr int Q_CHUNK = BM * 128;        // one 64-column box of Q: 16 KB
-constexpr int KV_CHUNK = BN * 128;       // one 64-column box of K or V: 8 KB
-constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
+constexpr int KV_CHUNK = BN * 128;  // one 64-column box of K or V: 8 KB
 constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
-constexpr int XS_BYTES = BM * BN * 4;    // partial-S exchange buffer (pair only)
+constexpr int XS_BYTES = BM * BN * 4;  // partial-S exchange buffer (pair only)
 
 template <bool kPair>
 struct Layout {
-  static constexpr int NST = kPair ? 3 : 4;  // K/V ring stages
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int NST = kPair ? 5 : 6;  // K/V ring stages
+  static constexpr int OFF_KV = 0;
   static constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
   static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_PMAX = OFF_XS + (kPair ? XS_BYTES : 0);  // [2 groups][128 rows] fp32
@@ -72,19 +80,19 @@ struct Layout {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-constexpr uint32_t TM_O = 0, TM_S0 = HS, TM_S1 = HS + BN, TM_COLS = 512;
+constexpr uint32_t TM_O = 0, TM_S0 = HS, TM_S1 = HS + BN, TM_Q = HS + 2 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-static_assert(TM_S1 + BN <= TM_COLS, "TMEM budget");
+static_assert(TM_Q + HS / 2 <= TM_COLS, "TMEM budget");
 
 template <int NST>
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (NST + s); }
-  __device__ uint32_t q() const { return base + 8 * (2 * NST); }
+  __device__ uint32_t q() const { return base + 8 * (2 * NST); }  // Q slice written to TMEM
   __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }
   __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 3 + b); }
   __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 5 + b); }
@@ -118,17 +126,44 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x on the special-function unit (subnormal results flush to 0; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Maximum of the scores sr[0, NC), whose key indices are kbase + c.  When
+// `masked`, scores outside the row's interval [lo, hi] are first set to -inf
+// (raw domain: the scale is positive).  Four partial maxima keep the
+// dependency chains short.
+template <int NC>
+__device__ __forceinline__ float mask_max(uint32_t* sr, int kbase, int lo, int hi, bool masked) {
+  if (masked) {
+    const int clo = lo - kbase, chi = hi - kbase;
+#pragma unroll
+    for (int c = 0; c < NC; ++c)
+      if (c < clo || c > chi) sr[c] = __float_as_uint(-CUDART_INF_F);
+  }
+  float m[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+#pragma unroll
+  for (int c = 0; c < NC; ++c) m[c & 3] = fmaxf(m[c & 3], __uint_as_float(sr[c]));
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+__device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
 template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const PrefillArgs a) {
   using LY = Layout<kPair>;
   constexpr int NST = LY::NST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + LY::OFF_Q, sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
+  const uint32_t sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
   const Bars<NST> bars{base + LY::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + LY::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
@@ -171,7 +206,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    mbar_init(bars.q(), 1);
+    mbar_init(bars.q(), 256);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bars.s_full(i), 1);
       mbar_init(bars.p_full(i), 256);
@@ -188,7 +223,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
@@ -203,86 +237,95 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // ring order: K_0, K_1, then V_j, K_{j+2} for j = 0 .. n-1
     if (n > 0) {
-      if (lane == 0) {
-        mbar_arrive_expect_tx(bars.q(), Q_BYTES);
-        for (int c = 0; c < HS / 64; ++c) tma_load_4d(sQ + c * Q_CHUNK, &tm_q, bars.q(), col0 + 64 * c, i0, hq, b);
-      }
-      __syncwarp();
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        const int k0 = (kt_lo + j) * BN;
-        for (int x = 0; x < 2 && ok; ++x) {
-          const int idx = 2 * j + x, s = idx % NST;
-          ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
-          if (ok && lane == 0) {
-            mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
-            const CUtensorMap* m = x ? &tm_v : &tm_k;
-            for (int c = 0; c < HS / 64; ++c)
-              tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
-          }
-          __syncwarp();
+      int idx = 0;
+      auto load = [&](int tile, bool is_v) {
+        const int s = idx % NST;
+        ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
+        if (ok && lane == 0) {
+          mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
+          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+          const int k0 = (kt_lo + tile) * BN;
+          for (int c = 0; c < HS / 64; ++c)
+            tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
         }
+        __syncwarp();
+        ++idx;
+      };
+      load(0, false);
+      if (n > 1 && ok) load(1, false);
+      for (int j = 0; j < n && ok; ++j) {
+        load(j, true);
+        if (j + 2 < n && ok) load(j + 2, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (n > 0) {
       bool ok = __all_sync(0xffffffffu, wait_bar(bars.q(), 0, abort_flag, err));
-      for (int j = 0; j <= n && ok; ++j) {
-        if (j < n) {
-          const int sb = j & 1, idx = 2 * j, s = idx % NST;
-          bool w = true;
-          if (j >= 2) w = wait_bar(bars.p_full(sb), ((j - 2) >> 1) & 1, abort_flag, err);  // S buffer read
-          w = w && wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err);
-          ok = __all_sync(0xffffffffu, w);
-          if (!ok) break;
-          if (lane == 0) {
-            tc_fence_after();
-            const uint32_t d = tmem + (sb ? TM_S1 : TM_S0);
+      // one K=16 step of S = Q K^T: Q from TMEM, K (K-major) from ring slot kslot
+      auto qk_step = [&](uint32_t dcol, uint32_t kslot, int kk) {
+        const int c = kk >> 2, sub = kk & 3;
+        const uint64_t bd = sdesc_sw128(kslot + c * KV_CHUNK + sub * 32, 16, 1024);
+        mma_bf16_ts(tmem + dcol, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+      };
+      int idx = 0;
+      for (int t = 0; t < 2 && t < n && ok; ++t) {
+        const int s = idx % NST;
+        ok = __all_sync(0xffffffffu, wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err));
+        if (!ok) break;
+        if (lane == 0) {
+          tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < HS / 16; ++kk) {
-              const int c = kk >> 2, sub = kk & 3;
-              const uint64_t ad = sdesc_sw128(sQ + c * Q_CHUNK + sub * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(sKV + s * KV_BYTES + c * KV_CHUNK + sub * 32, 16, 1024);
-              mma_bf16_ss(d, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(bars.s_full(sb));
-            mma_commit(bars.empty(s));
-          }
-          __syncwarp();
+          for (int kk = 0; kk < HS / 16; ++kk) qk_step(t ? TM_S1 : TM_S0, sKV + s * KV_BYTES, kk);
+          mma_commit(bars.s_full(t));
+          mma_commit(bars.empty(s));
         }
-        if (j >= 1) {
-          const int i = j - 1, pb = i & 1, idx = 2 * i + 1, s = idx % NST;
-          bool w = wait_bar(bars.p_full(pb), (i >> 1) & 1, abort_flag, err);
-          w = w && wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err);
-          ok = __all_sync(0xffffffffu, w);
-          if (!ok) break;
-          if (lane == 0) {
-            tc_fence_after();
+        __syncwarp();
+        ++idx;
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int pb = j & 1;
+        const bool next = j + 2 < n;
+        const int sv = idx % NST, sk = (idx + 1) % NST;
+        bool w = wait_bar(bars.p_full(pb), (j >> 1) & 1, abort_flag, err);  // P_j written, S_j read
+        w = w && wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err);
+        if (next) w = w && wait_bar(bars.full(sk), ((idx + 1) / NST) & 1, abort_flag, err);
+        ok = __all_sync(0xffffffffu, w);
+        if (!ok) break;
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t vslot = sKV + sv * KV_BYTES, kslot = sKV + sk * KV_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-              const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + kk * 32, 16, 1024);
-              // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
-              // 8-key row groups 1024 B apart
-              const uint64_t bd = sdesc_sw128(sKV + s * KV_BYTES + kk * 2048, KV_CHUNK, 1024);
-              mma_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int p = 0; p < BN / 16; ++p) {
+            // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
+            // 8-key row groups 1024 B apart
+            const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
+            mma_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV, (j > 0 || p > 0) ? 1u : 0u);
+            if (next) {
+#pragma unroll
+              for (int kk = 4 * p; kk < 4 * p + 4; ++kk) qk_step(pb ? TM_S1 : TM_S0, kslot, kk);
             }
-            mma_commit(bars.empty(s));
-            mma_commit(bars.pv_done(pb));
           }
-          __syncwarp();
+          mma_commit(bars.empty(sv));
+          mma_commit(bars.pv_done(pb));
+          if (next) {
+            mma_commit(bars.s_full(pb));
+            mma_commit(bars.empty(sk));
+          }
         }
+        __syncwarp();
+        idx += next ? 2 : 1;
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
-    // Two warpgroups; warp w serves TMEM lane quadrant (w % 4), i.e. one query
-    // row per thread, and group g = 0 / 1 handles score columns [32g, 32g + 32)
-    // of each key tile and output columns [128g, 128g + 128) of the slice.  The
-    // two threads of a row (warps w and w + 4) exchange their tile maxima
-    // through shared memory under a 64-thread named barrier per quadrant, so
-    // both take identical rescaling decisions.
+    // Warp w serves TMEM lane quadrant (w % 4), i.e. one query row per
+    // thread; the two threads of a row (one per group) take identical
+    // rescaling decisions because both see the same row maximum.
     const int grp = (warp - 2) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
@@ -301,18 +344,42 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       hi = min(hi, a.key_rows - 1);
     }
-    constexpr int HC = BN / 2;   // score columns per group
-    constexpr int OC = HS / 2;   // output columns per group
-    const int cb = grp * HC;     // first score column of this group
+    constexpr int HC = BN / 2;  // score columns per group
+    constexpr int OC = HS / 2;  // output columns per group
+    const int cb = grp * HC;    // first score column of this group
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     float* pmax = reinterpret_cast<float*>(gbase + LY::OFF_PMAX);  // [group][row]
-    const int bar_id = 1 + q4;   // named barrier of this quadrant's two warps
+    const int bar_id = 1 + q4;  // named barrier of this quadrant's two warps
     // my row slice of the exchange buffer, and the same slice in the peer's buffer
     const uint32_t xs_row = base + LY::OFF_XS + (r * BN + cb) * 4;
     const uint32_t xs_row_peer = kPair ? map_shared(xs_row, peer) : 0;
     const uint32_t xs_full_peer = kPair ? map_shared(bars.xs_full(), peer) : 0;
     const uint32_t xs_free_peer = kPair ? map_shared(bars.xs_free(), peer) : 0;
     const float c2 = a.scale_log2;
+
+    // this group's half of the row's Q slice -> TMEM (A operand of the score MMAs);
+    // 32-bit column c holds the bf16 pair (2c, 2c + 1), the lower index in the low half
+    if (n > 0) {
+      const uint4* qrow = reinterpret_cast<const uint4*>(
+          a.q + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0 + grp * (HS / 2));
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 v = row_ok ? __ldg(qrow + h * 8 + e) : make_uint4(0, 0, 0, 0);
+          w[4 * e] = v.x;
+          w[4 * e + 1] = v.y;
+          w[4 * e + 2] = v.z;
+          w[4 * e + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + TM_Q + grp * (HS / 4) + h * 32, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bars.q());
+    }
+
     // m_run is the reference maximum in the exp2 domain; l_run sums the
     // bf16-rounded probabilities of this group's columns (normalises O, which
     // the tensor core accumulates from the same rounded values); l_exact sums
@@ -324,10 +391,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ok = __all_sync(0xffffffffu, wait_bar(bars.s_full(sb), (t >> 1) & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[HC];
-      tmem_ld32(tmem + lane_off + (sb ? TM_S1 : TM_S0) + cb, sr);
-      tmem_ld_wait();
-      if (kPair) {
+      const uint32_t tS = tmem + lane_off + (sb ? TM_S1 : TM_S0);
+      const int k0 = (kt_lo + t) * BN;
+      // the masking pass runs only when some row of the warp needs it
+      const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
+      // sr[0, HC): this group's columns; single CTA: sr[HC, BN) the other group's
+      uint32_t sr[kPair ? HC : BN];
+      float mraw = -CUDART_INF_F;
+      if constexpr (kPair) {
+        tmem_ld32(tS + cb, sr);
+        tmem_ld_wait();
         // send my partial slice to the peer (once it has consumed the previous
         // one), then add the peer's partial slice to mine
         if (t > 0) {
@@ -351,23 +424,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           sr[c + 3] = __float_as_uint(__uint_as_float(sr[c + 3]) + v.w);
         }
         mbar_arrive_remote(xs_free_peer);
+        mraw = mask_max<HC>(sr, k0 + cb, lo, hi, masked);
+        // the two groups of this row agree on the tile maximum
+        pmax[grp * BM + r] = mraw;
+        named_sync(bar_id);
+        mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
+        named_sync(bar_id);
+      } else {
+        // both groups read the whole S row and take its maximum themselves
+        tmem_ld32(tS + cb, sr);
+        tmem_ld32(tS + (cb ^ HC), sr + HC);
+        tmem_ld_wait();
+        mraw = fmaxf(mask_max<HC>(sr, k0 + cb, lo, hi, masked), mask_max<HC>(sr + HC, k0 + (cb ^ HC), lo, hi, masked));
       }
-      // row interval: scores outside [lo, hi] become -inf (raw domain; scale > 0)
-      const int k0 = (kt_lo + t) * BN + cb;
-      const bool full = (k0 >= lo) && (k0 + HC - 1 <= hi);
-      float mraw = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < HC; ++c) {
-        float x = __uint_as_float(sr[c]);
-        if (!full && (k0 + c < lo || k0 + c > hi)) x = -CUDART_INF_F;
-        sr[c] = __float_as_uint(x);
-        mraw = fmaxf(mraw, x);
-      }
-      // the two groups of this row agree on the tile maximum
-      pmax[grp * BM + r] = mraw;
-      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
-      mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
-      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
       const float mt = mraw * c2;
       // lazy rescale: move the reference only when the maximum grows by > 2^8
       const bool move = (m_run == -CUDART_INF_F) ? (mt > -CUDART_INF_F) : (mt > m_run + kRescaleLog2);
@@ -395,19 +464,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       // probabilities exp2(s * scale_log2 - m_run), packed to bf16
       const float nm = (m_run == -CUDART_INF_F) ? 0.f : -m_run;
       uint32_t pk[HC / 2];
-      float lsum = 0.f, esum = 0.f;
+      float ls[2] = {0.f, 0.f}, es[2] = {0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < HC; c += 2) {
         const float x0 = __uint_as_float(sr[c]), x1 = __uint_as_float(sr[c + 1]);
-        const float p0 = exp2f(fmaf(x0, c2, nm));  // -inf -> 0
-        const float p1 = exp2f(fmaf(x1, c2, nm));
+        const float p0 = ex2(fmaf(x0, c2, nm));  // -inf -> 0
+        const float p1 = ex2(fmaf(x1, c2, nm));
         const uint32_t w = pack_bf16(p0, p1);
-        lsum += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
-        esum += p0 + p1;
+        ls[(c >> 1) & 1] += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+        es[(c >> 1) & 1] += p0 + p1;
         pk[c / 2] = w;
       }
-      l_run += lsum;
-      l_exact += esum;
+      l_run += ls[0] + ls[1];
+      l_exact += es[0] + es[1];
       if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
         ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
         if (!ok) break;
@@ -423,11 +492,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     // row sums of both groups
     pmax[grp * BM + r] = l_run;
-    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    named_sync(bar_id);
     const float l_tot = l_run + pmax[(grp ^ 1) * BM + r];
-    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    named_sync(bar_id);
     pmax[grp * BM + r] = l_exact;
-    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    named_sync(bar_id);
     const float e_tot = l_exact + pmax[(grp ^ 1) * BM + r];
     // epilogue: O / l -> bf16, this group's columns of the CTA's slice
     bool have_o = n > 0 && ok;
@@ -509,7 +578,7 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
 }
 
 template <bool kPair>
-cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
+cudaError_t launch_kind(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
                         cudaStream_t s) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -533,7 +602,7 @@ cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
     cfg.attrs = at;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair>, mq, mk, mv, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair>, mk, mv, a);
 }
 
 }  // namespace
@@ -541,17 +610,15 @@ cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   const uint64_t D = uint64_t(a.head_dim);
-  CUtensorMap mq, mk, mv;
-  // Q / out [B, C, Hq, D]: dims {D, C, Hq, B}
-  const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
-  const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
+  CUtensorMap mk, mv;
   // K / V: dims {D, key rows, Hkv, B} with the caller's strides
   const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
   const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
-  if (!make_map(&mq, a.q, qd, qs, BM) || !make_map(&mk, a.k, kd, ks, BN) || !make_map(&mv, a.v, kd, ks, BN))
-    return cudaErrorInvalidValue;
-  return a.head_dim == 256 ? launch_kind<false>(mq, mk, mv, a, s) : launch_kind<true>(mq, mk, mv, a, s);
+  if (!make_map(&mk, a.k, kd, ks, BN) || !make_map(&mv, a.v, kd, ks, BN)) return cudaErrorInvalidValue;
+  // Q rows are read with 16-byte loads
+  if (reinterpret_cast<uintptr_t>(a.q) & 15) return cudaErrorInvalidValue;
+  return a.head_dim == 256 ? launch_kind<false>(mk, mv, a, s) : launch_kind<true>(mk, mv, a, s);
 }
 
 }  // namespace swa
