@@ -64,41 +64,53 @@ constexpr int kThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
 constexpr int KV_CHUNK = BN * 128;  // one 64-column box of K or V: 8 KB
 constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
+constexpr int Q_CHUNK = BM * 128;  // one 64-column box of Q: 16 KB
+constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
 constexpr int XS_BYTES = BM * BN * 4;  // partial-S exchange buffer (pair only)
 
-template <bool kPair>
+// kSm2: the CTA pair shares its MMAs (cta_group::2) and each CTA holds half
+// of every K/V tile: 32 keys of K, 128 head-dimension columns of V.  Its Q
+// slice stays in shared memory, which frees tensor memory for a third S buffer.
+template <bool kPair, bool kSm2>
 struct Layout {
-  static constexpr int NST = kPair ? 5 : 6;  // K/V ring stages
-  static constexpr int OFF_KV = 0;
-  static constexpr int OFF_P = OFF_KV + NST * KV_BYTES;
+  static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;  // one ring slot
+  static constexpr int NST = kPair ? 5 : (kSm2 ? 8 : 6);       // K/V ring stages
+  static constexpr int NS = kSm2 ? 3 : 2;                      // S buffers in TMEM
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + (kSm2 ? Q_BYTES : 0);
+  static constexpr int OFF_P = OFF_KV + NST * SLOT;
   static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
   static constexpr int OFF_PMAX = OFF_XS + (kPair ? XS_BYTES : 0);  // [2 groups][128 rows] fp32
   static constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
-  static constexpr int N_BARS = 2 * NST + 10;
+  static constexpr int N_BARS = 2 * NST + 11;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-constexpr uint32_t TM_O = 0, TM_S0 = HS, TM_S1 = HS + BN, TM_Q = HS + 2 * BN, TM_COLS = 512;
+// TMEM columns: O, then the S buffers (TM_S + b * BN), then the Q slice when
+// it lives in tensor memory (single CTA: after two S buffers)
+constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
+constexpr uint32_t IDESC_QK2 = idesc_bf16_f32(2 * BM, BN, false);  // CTA pair: 256 query rows
+constexpr uint32_t IDESC_PV2 = idesc_bf16_f32(2 * BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-static_assert(TM_Q + HS / 2 <= TM_COLS, "TMEM budget");
+static_assert(TM_Q + HS / 2 <= TM_COLS && TM_S + 3 * BN <= TM_COLS, "TMEM budget");
 
 template <int NST>
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (NST + s); }
-  __device__ uint32_t q() const { return base + 8 * (2 * NST); }  // Q slice written to TMEM
-  __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }
-  __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 3 + b); }
-  __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 5 + b); }
-  __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 7); }
-  __device__ uint32_t xs_full() const { return base + 8 * (2 * NST + 8); }  // peer's partial arrived
-  __device__ uint32_t xs_free() const { return base + 8 * (2 * NST + 9); }  // peer consumed my partial
+  __device__ uint32_t q() const { return base + 8 * (2 * NST); }  // Q slice ready for the MMAs
+  __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }  // b < 3
+  __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 4 + b); }
+  __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 6 + b); }
+  __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 8); }
+  __device__ uint32_t xs_full() const { return base + 8 * (2 * NST + 9); }  // peer's partial arrived
+  __device__ uint32_t xs_free() const { return base + 8 * (2 * NST + 10); }  // peer consumed my partial
 };
 
 // Bounded wait on one phase of an mbarrier.  Gives up when another role has
@@ -153,17 +165,19 @@ __device__ __forceinline__ float mask_max(uint32_t* sr, int kbase, int lo, int h
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
-template <bool kPair>
+template <bool kPair, bool kSm2>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const PrefillArgs a) {
-  using LY = Layout<kPair>;
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  using LY = Layout<kPair, kSm2>;
+  static_assert(!(kPair && kSm2), "the pair MMA serves head size 256 only");
   constexpr int NST = LY::NST;
+  constexpr int NS = LY::NS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
+  const uint32_t sQ = base + LY::OFF_Q, sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
   const Bars<NST> bars{base + LY::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + LY::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
@@ -174,6 +188,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const int peer = half ^ 1;
   const int col0 = half * HS;
   const int hq = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
+  // kSm2: the cluster's two CTAs are query heads 2g and 2g + 1 of one KV head
+  // (same rows, same key tiles); the even CTA issues the pair MMAs
+  const int crank = kSm2 ? int(cluster_ctarank()) : 0;
+  const bool issuer = crank == 0;
   const int qt = blockIdx.y, b = blockIdx.z;
   const int hk = hq / (a.q_heads / a.kv_heads);
   const int i0 = qt * BM;
@@ -206,10 +224,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    mbar_init(bars.q(), 256);
+    // single CTA: the softmax threads copy Q into TMEM; kSm2: both CTAs' Q
+    // tiles complete on the issuing CTA's barrier
+    mbar_init(bars.q(), kSm2 ? 1 : 256);
+    for (int i = 0; i < 3; ++i) mbar_init(bars.s_full(i), 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bars.s_full(i), 1);
-      mbar_init(bars.p_full(i), 256);
+      // kSm2: the issuing CTA also counts the one arrival its peer forwards
+      mbar_init(bars.p_full(i), kSm2 && issuer ? 257 : 256);
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
@@ -219,15 +240,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
-    tmem_relinquish();
+    if (kSm2) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+      tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
+    if (kSm2) prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
   tc_fence_before();
-  if (kPair) {
+  if (kPair || kSm2) {
     cluster_sync();  // the peer's barriers are initialised before any remote arrive
   } else {
     __syncthreads();
@@ -237,88 +264,133 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // ring order: K_0, K_1, then V_j, K_{j+2} for j = 0 .. n-1
+    // ring order: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for j = 0 .. n-1
     if (n > 0) {
       bool ok = true;
       int idx = 0;
+      if (kSm2 && lane == 0) {  // this CTA's Q rows; both tiles complete on the issuer's barrier
+        if (issuer) mbar_arrive_expect_tx(bars.q(), 2 * Q_BYTES);
+        for (int c = 0; c < HS / 64; ++c)
+          tma_load_4d_pair(sQ + c * Q_CHUNK, &tm_q, map_shared(bars.q(), 0), col0 + 64 * c, i0, hq, b);
+      }
       auto load = [&](int tile, bool is_v) {
         const int s = idx % NST;
         ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
         if (ok && lane == 0) {
-          mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
-          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
           const int k0 = (kt_lo + tile) * BN;
-          for (int c = 0; c < HS / 64; ++c)
-            tma_load_4d(sKV + s * KV_BYTES + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
+          const uint32_t dst = sKV + s * LY::SLOT;
+          if constexpr (kSm2) {
+            // this CTA's half; both halves complete on the issuing CTA's barrier
+            const uint32_t bar = map_shared(bars.full(s), 0);
+            if (issuer) mbar_arrive_expect_tx(bars.full(s), 2 * LY::SLOT);
+            if (is_v) {
+              for (int c = 0; c < 2; ++c)  // head-dimension columns [128 crank, 128 crank + 128)
+                tma_load_4d_pair(dst + c * KV_CHUNK, &tm_v, bar, 128 * crank + 64 * c, k0, hk, b);
+            } else {
+              for (int c = 0; c < HS / 64; ++c)  // keys [k0 + 32 crank, k0 + 32 crank + 32)
+                tma_load_4d_pair(dst + c * (KV_CHUNK / 2), &tm_k, bar, 64 * c, k0 + (BN / 2) * crank, hk, b);
+            }
+          } else {
+            mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
+            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+            for (int c = 0; c < HS / 64; ++c)
+              tma_load_4d(dst + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
+          }
         }
         __syncwarp();
         ++idx;
       };
-      load(0, false);
-      if (n > 1 && ok) load(1, false);
+      for (int t = 0; t < NS && t < n && ok; ++t) load(t, false);
       for (int j = 0; j < n && ok; ++j) {
         load(j, true);
-        if (j + 2 < n && ok) load(j + 2, false);
+        if (j + NS < n && ok) load(j + NS, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (n > 0) {
-      bool ok = __all_sync(0xffffffffu, wait_bar(bars.q(), 0, abort_flag, err));
-      // one K=16 step of S = Q K^T: Q from TMEM, K (K-major) from ring slot kslot
-      auto qk_step = [&](uint32_t dcol, uint32_t kslot, int kk) {
+    // one thread issues every MMA; the other lanes of the warp stay idle
+    if (n > 0 && issuer && lane == 0) {
+      bool ok = wait_bar<kSm2>(bars.q(), 0, abort_flag, err);
+      // kK: bytes between the 64-column boxes of a K slot
+      constexpr int kK = kSm2 ? KV_CHUNK / 2 : KV_CHUNK;
+      // one K=16 step of S_b = Q K^T into S buffer b; K (K-major) from ring slot
+      // kslot; Q from TMEM (single CTA) or from shared memory (kSm2)
+      auto qk_step = [&](int sbuf, uint32_t kslot, int kk) {
         const int c = kk >> 2, sub = kk & 3;
-        const uint64_t bd = sdesc_sw128(kslot + c * KV_CHUNK + sub * 32, 16, 1024);
-        mma_bf16_ts(tmem + dcol, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+        const uint64_t bd = sdesc_sw128(kslot + c * kK + sub * 32, 16, 1024);
+        const uint32_t d = tmem + TM_S + sbuf * BN;
+        if (kSm2)
+          mma_pair_bf16_ss(d, sdesc_sw128(sQ + c * Q_CHUNK + sub * 32, 16, 1024), bd, IDESC_QK2, kk > 0 ? 1u : 0u);
+        else
+          mma_bf16_ts(d, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+      };
+      // completion of the MMAs issued so far, on `bar` of both CTAs (kSm2) or of this CTA
+      auto commit = [&](uint32_t bar) {
+        if (kSm2)
+          mma_pair_commit(bar, 0x3);
+        else
+          mma_commit(bar);
       };
       int idx = 0;
-      for (int t = 0; t < 2 && t < n && ok; ++t) {
+      for (int t = 0; t < NS && t < n && ok; ++t) {
         const int s = idx % NST;
-        ok = __all_sync(0xffffffffu, wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err));
+        ok = wait_bar(bars.full(s), (idx / NST) & 1, abort_flag, err);
         if (!ok) break;
-        if (lane == 0) {
-          tc_fence_after();
+        tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < HS / 16; ++kk) qk_step(t ? TM_S1 : TM_S0, sKV + s * KV_BYTES, kk);
-          mma_commit(bars.s_full(t));
-          mma_commit(bars.empty(s));
-        }
-        __syncwarp();
+        for (int kk = 0; kk < HS / 16; ++kk) qk_step(t, sKV + s * LY::SLOT, kk);
+        commit(bars.s_full(t));
+        commit(bars.empty(s));
         ++idx;
       }
       for (int j = 0; j < n && ok; ++j) {
         const int pb = j & 1;
-        const bool next = j + 2 < n;
+        const bool next = j + NS < n;  // S_{j+NS} goes to the buffer S_j came from
+        const int sbuf = j % NS;
         const int sv = idx % NST, sk = (idx + 1) % NST;
-        bool w = wait_bar(bars.p_full(pb), (j >> 1) & 1, abort_flag, err);  // P_j written, S_j read
-        w = w && wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err);
-        if (next) w = w && wait_bar(bars.full(sk), ((idx + 1) / NST) & 1, abort_flag, err);
-        ok = __all_sync(0xffffffffu, w);
-        if (!ok) break;
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t vslot = sKV + sv * KV_BYTES, kslot = sKV + sk * KV_BYTES;
+        // P_j written (so S_j read), V_j and K_{j+NS} loaded: one round of polls,
+        // then bounded waits for whatever is still pending
+        const bool pf = kSm2 ? mbar_try_wait_cluster(bars.p_full(pb), (j >> 1) & 1)
+                             : mbar_try_wait(bars.p_full(pb), (j >> 1) & 1);
+        const bool vf = mbar_try_wait(bars.full(sv), (idx / NST) & 1);
+        const bool kf = !next || mbar_try_wait(bars.full(sk), ((idx + 1) / NST) & 1);
+        if (!(pf & vf & kf)) {
+          ok = wait_bar<kSm2>(bars.p_full(pb), (j >> 1) & 1, abort_flag, err) &&
+               wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err) &&
+               (!next || wait_bar(bars.full(sk), ((idx + 1) / NST) & 1, abort_flag, err));
+          if (!ok) break;
+        }
+        tc_fence_after();
+        const uint32_t vslot = sKV + sv * LY::SLOT, kslot = sKV + sk * LY::SLOT;
 #pragma unroll
-          for (int p = 0; p < BN / 16; ++p) {
-            // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
-            // 8-key row groups 1024 B apart
-            const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
+        for (int p = 0; p < BN / 16; ++p) {
+          // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
+          // 8-key row groups 1024 B apart
+          const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
+          if (kSm2)
+            mma_pair_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV2, (j > 0 || p > 0) ? 1u : 0u);
+          else
             mma_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV, (j > 0 || p > 0) ? 1u : 0u);
-            if (next) {
-#pragma unroll
-              for (int kk = 4 * p; kk < 4 * p + 4; ++kk) qk_step(pb ? TM_S1 : TM_S0, kslot, kk);
-            }
-          }
-          mma_commit(bars.empty(sv));
-          mma_commit(bars.pv_done(pb));
           if (next) {
-            mma_commit(bars.s_full(pb));
-            mma_commit(bars.empty(sk));
+#pragma unroll
+            for (int kk = 4 * p; kk < 4 * p + 4; ++kk) qk_step(sbuf, kslot, kk);
           }
         }
-        __syncwarp();
+        if (next) commit(bars.s_full(sbuf));
+        commit(bars.pv_done(pb));
+        commit(bars.empty(sv));
+        if (next) commit(bars.empty(sk));
         idx += next ? 2 : 1;
+      }
+    } else if (kSm2 && n > 0 && !issuer) {
+      // the peer CTA forwards each P_j's readiness to the issuing CTA with one
+      // cluster-scope arrival
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        ok = __all_sync(0xffffffffu, wait_bar(bars.p_full(j & 1), (j >> 1) & 1, abort_flag, err));
+        if (ok && lane == 0) mbar_arrive_remote(map_shared(bars.p_full(j & 1), 0));
+        __syncwarp();
       }
     }
   } else {
@@ -359,7 +431,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
 
     // this group's half of the row's Q slice -> TMEM (A operand of the score MMAs);
     // 32-bit column c holds the bf16 pair (2c, 2c + 1), the lower index in the low half
-    if (n > 0) {
+    if (!kSm2 && n > 0) {
       const uint4* qrow = reinterpret_cast<const uint4*>(
           a.q + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0 + grp * (HS / 2));
 #pragma unroll
@@ -387,11 +459,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
-      const int sb = t & 1, pb = t & 1;
-      ok = __all_sync(0xffffffffu, wait_bar(bars.s_full(sb), (t >> 1) & 1, abort_flag, err));
+      const int sb = t % NS, pb = t & 1;
+      ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tmem + lane_off + (sb ? TM_S1 : TM_S0);
+      const uint32_t tS = tmem + lane_off + TM_S + sb * BN;
       const int k0 = (kt_lo + t) * BN;
       // the masking pass runs only when some row of the warp needs it
       const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
@@ -442,7 +514,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       const bool move = (m_run == -CUDART_INF_F) ? (mt > -CUDART_INF_F) : (mt > m_run + kRescaleLog2);
       const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
       if (__any_sync(0xffffffffu, rescale)) {
-        ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
+        ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
         if (!ok) break;
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
@@ -478,7 +550,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       l_run += ls[0] + ls[1];
       l_exact += es[0] + es[1];
       if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
-        ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
+        ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
         if (!ok) break;
       }
       uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
@@ -501,7 +573,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     // epilogue: O / l -> bf16, this group's columns of the CTA's slice
     bool have_o = n > 0 && ok;
     if (have_o)
-      have_o = __all_sync(0xffffffffu, wait_bar(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
+      have_o = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
     tc_fence_after();
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0;
@@ -532,8 +604,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   if (*abort_flag) {
     // let the MMAs and TMA copies this CTA issued finish before TMEM and
     // shared memory are released
-    if (warp == 1 && lane == 0) {
-      mma_commit(bars.teardown());
+    if (warp == 1 && lane == 0 && issuer) {
+      if (kSm2)
+        mma_pair_commit(bars.teardown(), 0x1);
+      else
+        mma_commit(bars.teardown());
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bars.teardown(), 0) && globaltimer_ns() - t0 < kTimeoutNs) {
       }
@@ -545,9 +620,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     }
     __syncthreads();
   }
-  if (kPair) cluster_sync();  // the peer no longer writes into this CTA's shared memory
+  if (kPair || kSm2) cluster_sync();  // the peer no longer reads or writes this CTA's shared memory
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, TM_COLS);
+  if (warp == 1) {
+    if (kSm2)
+      tmem_dealloc_pair(tmem, TM_COLS);
+    else
+      tmem_dealloc(tmem, TM_COLS);
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -577,24 +657,24 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   return r == CUDA_SUCCESS;
 }
 
-template <bool kPair>
-cudaError_t launch_kind(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
+template <bool kPair, bool kSm2>
+cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
                         cudaStream_t s) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Layout<kPair>::SMEM);
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair, kSm2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Layout<kPair, kSm2>::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int nqt = (a.chunk_len + BM - 1) / BM;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.q_heads * (kPair ? 2 : 1), nqt, a.batch);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Layout<kPair>::SMEM;
+  cfg.dynamicSmemBytes = Layout<kPair, kSm2>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
-  if (kPair) {
+  if (kPair || kSm2) {
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = 2;
     at[0].val.clusterDim.y = 1;
@@ -602,7 +682,7 @@ cudaError_t launch_kind(const CUtensorMap& mk, const CUtensorMap& mv, const Pref
     cfg.attrs = at;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair>, mk, mv, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair, kSm2>, mq, mk, mv, a);
 }
 
 }  // namespace
@@ -610,15 +690,22 @@ cudaError_t launch_kind(const CUtensorMap& mk, const CUtensorMap& mv, const Pref
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   const uint64_t D = uint64_t(a.head_dim);
-  CUtensorMap mk, mv;
+  CUtensorMap mq, mk, mv;
+  // query heads 2g and 2g + 1 share a KV head when the group size is even:
+  // their CTAs then form a pair that shares its MMAs and K/V tiles
+  const bool sm2 = a.head_dim == 256 && (a.q_heads / a.kv_heads) % 2 == 0;
   // K / V: dims {D, key rows, Hkv, B} with the caller's strides
   const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
   const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
-  if (!make_map(&mk, a.k, kd, ks, BN) || !make_map(&mv, a.v, kd, ks, BN)) return cudaErrorInvalidValue;
-  // Q rows are read with 16-byte loads
-  if (reinterpret_cast<uintptr_t>(a.q) & 15) return cudaErrorInvalidValue;
-  return a.head_dim == 256 ? launch_kind<false>(mk, mv, a, s) : launch_kind<true>(mk, mv, a, s);
+  if (!make_map(&mk, a.k, kd, ks, sm2 ? BN / 2 : BN) || !make_map(&mv, a.v, kd, ks, BN)) return cudaErrorInvalidValue;
+  // Q [B, C, Hq, D]: dims {D, C, Hq, B} (tiles of 128 rows; the pair kernel
+  // loads them with TMA, the others read rows with 16-byte loads)
+  const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
+  const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
+  if (!make_map(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
+  if (a.head_dim == 512) return launch_kind<true, false>(mq, mk, mv, a, s);
+  return sm2 ? launch_kind<false, true>(mq, mk, mv, a, s) : launch_kind<false, false>(mq, mk, mv, a, s);
 }
 
 }  // namespace swa
