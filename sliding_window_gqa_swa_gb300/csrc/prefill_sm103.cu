@@ -70,16 +70,17 @@ constexpr int XS_BYTES = BM * BN * 4;  // partial-S exchange buffer (pair only)
 
 // kSm2: the CTA pair shares its MMAs (cta_group::2) and each CTA holds half
 // of every K/V tile: 32 keys of K, 128 head-dimension columns of V.  Its Q
-// slice stays in shared memory, which frees tensor memory for a third S buffer.
+// slice stays in shared memory, which frees tensor memory for a third S buffer;
+// P lives in tensor memory (two 32-column buffers after the S buffers).
 template <bool kPair, bool kSm2>
 struct Layout {
   static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;  // one ring slot
-  static constexpr int NST = kPair ? 5 : (kSm2 ? 8 : 6);       // K/V ring stages
+  static constexpr int NST = kPair ? 5 : (kSm2 ? 10 : 6);      // K/V ring stages
   static constexpr int NS = kSm2 ? 3 : 2;                      // S buffers in TMEM
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + (kSm2 ? Q_BYTES : 0);
   static constexpr int OFF_P = OFF_KV + NST * SLOT;
-  static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_XS = OFF_P + (kSm2 ? 0 : 2 * P_BYTES);
   static constexpr int OFF_PMAX = OFF_XS + (kPair ? XS_BYTES : 0);  // [2 groups][128 rows] fp32
   static constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
   static constexpr int N_BARS = 2 * NST + 11;
@@ -90,14 +91,14 @@ struct Layout {
 
 // TMEM columns: O, then the S buffers (TM_S + b * BN), then the Q slice when
 // it lives in tensor memory (single CTA: after two S buffers)
-constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_COLS = 512;
+constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_P = HS + 3 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
 constexpr uint32_t IDESC_QK2 = idesc_bf16_f32(2 * BM, BN, false);  // CTA pair: 256 query rows
 constexpr uint32_t IDESC_PV2 = idesc_bf16_f32(2 * BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-static_assert(TM_Q + HS / 2 <= TM_COLS && TM_S + 3 * BN <= TM_COLS, "TMEM budget");
+static_assert(TM_Q + HS / 2 <= TM_COLS && TM_P + BN <= TM_COLS, "TMEM budget");
 
 template <int NST>
 struct Bars {
@@ -366,12 +367,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int p = 0; p < BN / 16; ++p) {
           // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
           // 8-key row groups 1024 B apart
-          const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
-          if (kSm2)
-            mma_pair_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV2, (j > 0 || p > 0) ? 1u : 0u);
+          if (kSm2)  // P_j from TMEM: 8 columns (16 keys) per step
+            mma_pair_bf16_ts(tmem + TM_O, tmem + TM_P + pb * (BN / 2) + p * 8, bd, IDESC_PV2,
+                             (j > 0 || p > 0) ? 1u : 0u);
           else
-            mma_bf16_ss(tmem + TM_O, ad, bd, IDESC_PV, (j > 0 || p > 0) ? 1u : 0u);
+            mma_bf16_ss(tmem + TM_O, sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024), bd, IDESC_PV,
+                        (j > 0 || p > 0) ? 1u : 0u);
           if (next) {
 #pragma unroll
             for (int kk = 4 * p; kk < 4 * p + 4; ++kk) qk_step(sbuf, kslot, kk);
@@ -553,12 +555,18 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
         if (!ok) break;
       }
-      uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
+      if constexpr (kSm2) {
+        // this group's 32 keys = 16 bf16 pairs of the row's P buffer in TMEM
+        tmem_st16(tmem + lane_off + TM_P + pb * (BN / 2) + grp * (HC / 2), pk);
+        tmem_st_wait();
+      } else {
+        uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(prow + (((grp * 4 + j) ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-      fence_proxy_async_smem();
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(prow + (((grp * 4 + j) ^ (r & 7)) << 4)) =
+              make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       mbar_arrive(bars.p_full(pb));
     }
