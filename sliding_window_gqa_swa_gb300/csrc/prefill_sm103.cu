@@ -60,13 +60,15 @@ using namespace ptx;
 constexpr int BM = kPlanBM;    // 128 query rows per CTA
 constexpr int BN = 64;         // keys per tile
 constexpr int HS = 256;        // head-dimension slice per CTA
-constexpr int kThreads = 320;  // TMA warp, MMA warp, two softmax warpgroups
+// TMA warp, MMA warp, two softmax warpgroups; head size 512 adds a warp that
+// forwards the partial-score exchange's "buffer consumed" signal to the peer
+constexpr int threads_of(bool pair) { return pair ? 352 : 320; }
 constexpr int KV_CHUNK = BN * 128;  // one 64-column box of K or V: 8 KB
 constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
 constexpr int Q_CHUNK = BM * 128;  // one 64-column box of Q: 16 KB
 constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
-constexpr int XS_BYTES = BM * BN * 4;  // partial-S exchange buffer (pair only)
+constexpr int XS_BYTES = BM * BN * 4;  // one partial-S exchange buffer (head size 512; two of them)
 
 // kSm2: the CTA pair shares its MMAs (cta_group::2) and each CTA holds half
 // of every K/V tile: 32 keys of K, 128 head-dimension columns of V.  Its Q
@@ -75,15 +77,15 @@ constexpr int XS_BYTES = BM * BN * 4;  // partial-S exchange buffer (pair only)
 template <bool kPair, bool kSm2>
 struct Layout {
   static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;  // one ring slot
-  static constexpr int NST = kPair ? 5 : (kSm2 ? 10 : 6);      // K/V ring stages
+  static constexpr int NST = kPair ? 4 : (kSm2 ? 10 : 6);      // K/V ring stages
   static constexpr int NS = kSm2 ? 3 : 2;                      // S buffers in TMEM
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + (kSm2 ? Q_BYTES : 0);
   static constexpr int OFF_P = OFF_KV + NST * SLOT;
   static constexpr int OFF_XS = OFF_P + (kSm2 ? 0 : 2 * P_BYTES);
-  static constexpr int OFF_PMAX = OFF_XS + (kPair ? XS_BYTES : 0);  // [2 groups][128 rows] fp32
+  static constexpr int OFF_PMAX = OFF_XS + (kPair ? 2 * XS_BYTES : 0);  // [2 groups][128 rows] fp32
   static constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
-  static constexpr int N_BARS = 2 * NST + 11;
+  static constexpr int N_BARS = 2 * NST + 15;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -110,8 +112,11 @@ struct Bars {
   __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 4 + b); }
   __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 6 + b); }
   __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 8); }
-  __device__ uint32_t xs_full() const { return base + 8 * (2 * NST + 9); }  // peer's partial arrived
-  __device__ uint32_t xs_free() const { return base + 8 * (2 * NST + 10); }  // peer consumed my partial
+  // head size 512, exchange buffer b: the peer's partial arrived (transaction
+  // bytes of its stores), this CTA consumed it, the peer consumed this CTA's
+  __device__ uint32_t xs_full(int b) const { return base + 8 * (2 * NST + 9 + b); }
+  __device__ uint32_t xs_cons(int b) const { return base + 8 * (2 * NST + 11 + b); }
+  __device__ uint32_t xs_free(int b) const { return base + 8 * (2 * NST + 13 + b); }
 };
 
 // Bounded wait on one phase of an mbarrier.  Gives up when another role has
@@ -167,7 +172,7 @@ __device__ __forceinline__ float mask_max(uint32_t* sr, int kbase, int lo, int h
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 template <bool kPair, bool kSm2>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of(kPair), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
   using LY = Layout<kPair, kSm2>;
@@ -235,8 +240,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
-    mbar_init(bars.xs_full(), 256);
-    mbar_init(bars.xs_free(), 256);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars.xs_full(i), 1);
+      mbar_init(bars.xs_cons(i), 256);
+      mbar_init(bars.xs_free(i), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -395,6 +403,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
       }
     }
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ exchange forwarder (head size 512)
+    // this CTA consumed the peer's partial in buffer t & 1: the peer may refill it
+    bool ok = true;
+    for (int t = 0; t < n && ok; ++t) {
+      ok = __all_sync(0xffffffffu, wait_bar(bars.xs_cons(t & 1), (t >> 1) & 1, abort_flag, err));
+      if (ok && lane == 0) mbar_arrive_remote(map_shared(bars.xs_free(t & 1), peer));
+      __syncwarp();
+    }
   } else {
     // ------------------------------------------------------------ softmax
     // Warp w serves TMEM lane quadrant (w % 4), i.e. one query row per
@@ -427,8 +444,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // my row slice of the exchange buffer, and the same slice in the peer's buffer
     const uint32_t xs_row = base + LY::OFF_XS + (r * BN + cb) * 4;
     const uint32_t xs_row_peer = kPair ? map_shared(xs_row, peer) : 0;
-    const uint32_t xs_full_peer = kPair ? map_shared(bars.xs_full(), peer) : 0;
-    const uint32_t xs_free_peer = kPair ? map_shared(bars.xs_free(), peer) : 0;
+
     const float c2 = a.scale_log2;
 
     // this group's half of the row's Q slice -> TMEM (A operand of the score MMAs);
@@ -475,20 +491,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if constexpr (kPair) {
         tmem_ld32(tS + cb, sr);
         tmem_ld_wait();
-        // send my partial slice to the peer (once it has consumed the previous
-        // one), then add the peer's partial slice to mine
-        if (t > 0) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(), (t - 1) & 1, abort_flag, err));
+        // send my partial slice into the peer's exchange buffer xb (once the peer
+        // has consumed what this CTA sent there two tiles ago); the stores count
+        // their bytes on the peer's xs_full(xb)
+        const int xb = t & 1;
+        if (t >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(xb), ((t >> 1) - 1) & 1, abort_flag, err));
           if (!ok) break;
         }
+        const uint32_t fbar = map_shared(bars.xs_full(xb), peer);
 #pragma unroll
         for (int c = 0; c < HC; c += 4)
-          st_dsmem_f32x4(xs_row_peer + c * 4, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]),
-                         __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-        mbar_arrive_remote(xs_full_peer);
-        ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_full(), t & 1, abort_flag, err));
+          st_async_u32x4(xs_row_peer + xb * XS_BYTES + c * 4, sr[c], sr[c + 1], sr[c + 2], sr[c + 3], fbar);
+        // this CTA receives one whole partial tile per tile
+        if (threadIdx.x == 64) mbar_arrive_expect_tx(bars.xs_full(xb), XS_BYTES);
+        ok = __all_sync(0xffffffffu, wait_bar(bars.xs_full(xb), (t >> 1) & 1, abort_flag, err));
         if (!ok) break;
-        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS) + r * BN + cb;
+        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS + xb * XS_BYTES) + r * BN + cb;
 #pragma unroll
         for (int c = 0; c < HC; c += 4) {
           const float4 v = *reinterpret_cast<const float4*>(xr + c);
@@ -497,7 +516,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           sr[c + 2] = __float_as_uint(__uint_as_float(sr[c + 2]) + v.z);
           sr[c + 3] = __float_as_uint(__uint_as_float(sr[c + 3]) + v.w);
         }
-        mbar_arrive_remote(xs_free_peer);
+        mbar_arrive(bars.xs_cons(xb));  // the forwarding warp tells the peer
         mraw = mask_max<HC>(sr, k0 + cb, lo, hi, masked);
         // the two groups of this row agree on the tile maximum
         pmax[grp * BM + r] = mraw;
@@ -678,7 +697,7 @@ cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
   const int nqt = (a.chunk_len + BM - 1) / BM;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.q_heads * (kPair ? 2 : 1), nqt, a.batch);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_of(kPair));
   cfg.dynamicSmemBytes = Layout<kPair, kSm2>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];

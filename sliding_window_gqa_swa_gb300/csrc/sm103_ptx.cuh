@@ -127,6 +127,15 @@ __device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float a, float b, 
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
 }
+// 16-byte store into another CTA's shared memory whose completion is counted
+// (as transaction bytes) on that CTA's mbarrier `bar` (cluster addresses).
+__device__ __forceinline__ void st_async_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                               uint32_t bar) {
+  asm volatile("st.async.weak.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier (remote) shared-memory writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
