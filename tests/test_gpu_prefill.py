@@ -75,6 +75,10 @@ CASES = {
     "vlm_d512": (4106, 1, 4, 2, 512, 32, 256, 128, 0, {0: [(10, 100), (150, 200)]}),
     "causal_wide_window": (4108, 1, 2, 1, 256, 2000, 333, 333, 3, None),
     "causal_window_below_tile": (4109, 2, 2, 2, 256, 20, 200, 72, 11, None),
+    # head size 256 runs query heads 2g and 2g + 1 as one CTA pair when the group
+    # size is even, and one CTA per head otherwise
+    "gqa3_single_cta": (4111, 1, 6, 2, 256, 96, 260, 260, 5, None),
+    "gqa4_pairs": (4112, 1, 8, 2, 256, 96, 260, 130, 5, None),
 }
 
 # query scale that spreads scores over a wide range, so the running maximum of
