@@ -157,6 +157,8 @@ decode_kernel(const DecodeArgs a) {
   const uint32_t sring = smem_u32(smem);
   const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kStages);
 
+  // the next kernel of the stream may start its own cache prefetch now
+  if (tid == 0) pdl_launch_dependents();
   swa_device_state* st = a.state;
   const long long slab = (((long long)a.layer * a.batch + b) * a.kv_heads + h) * (long long)R * D;
   uint16_t* Kc = a.k_cache + slab;
@@ -196,6 +198,10 @@ decode_kernel(const DecodeArgs a) {
         bulk_load(sring + c * kStageBytes + CHUNK_BYTES, Vc + row * D, bytes, bar_full0 + 8 * c);
       }
     }
+    // everything above read only this layer's cache rows, which no earlier
+    // kernel of the stream writes; the inputs below may come from the kernel
+    // launched just before this one
+    pdl_wait();
     // the new row, the mask bytes of the range
     for (int i = lane; i < D / 8; i += 32) {
       reinterpret_cast<uint4*>(kn_s)[i] = reinterpret_cast<const uint4*>(kn)[i];
@@ -208,6 +214,7 @@ decode_kernel(const DecodeArgs a) {
   // load overlaps the state, mask and K/V round trip
   uint4 qraw[G][V16];
   if (warp < kComputeWarps) {
+    pdl_wait();
     const int li = lane % LPR;
     const uint16_t* qp = a.q + ((long long)b * a.q_heads + (long long)h * G) * D;
 #pragma unroll
@@ -642,14 +649,19 @@ cudaError_t launch_t(const DecodeArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(32 * (NW + 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attrs[1];
+  cudaLaunchAttribute attrs[2];
+  // programmatic dependent launch: the kernel prefetches its cache rows while
+  // the previous kernel of the stream finishes (it waits before reading inputs)
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 1;
   if (a.cluster) {
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = a.nsplit;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
+    attrs[1].id = cudaLaunchAttributeClusterDimension;
+    attrs[1].val.clusterDim.x = a.nsplit;
+    attrs[1].val.clusterDim.y = 1;
+    attrs[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   return cudaLaunchKernelEx(&cfg, decode_kernel<D, G, NW>, a);
 }
