@@ -261,6 +261,14 @@ SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_head
  * workspace: >= swa_decode_workspace_bytes device bytes, zero-filled before
  * its first use; each call leaves it ready for the next.  Calls that overlap
  * on the GPU need separate workspaces.
+ * Launch chaining: the kernel is launched with programmatic dependent launch.
+ * It may start while the previous kernel of the stream is still running and
+ * read this layer's cache rows then; it waits for that kernel before reading
+ * q, k_new, v_new, the mask and the cache state, and before writing anything.
+ * So the kernel launched just before it on the stream must not write this
+ * layer's cache rows (swa_build_mask, projections and the other layers'
+ * swa_decode calls do not; swa_roll and swa_compact are followed by the
+ * step's swa_build_mask anyway).
  * Supported: head_dim 64, 128, 256 or 512; Hq / Hkv in {1, 2, 4, 8}. */
 SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
                               const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
