@@ -108,3 +108,63 @@ class CompactModel:
             raise ValueError("the cache holds positions outside the given array")
         out[ok] = full[idx]
         return out
+
+
+class RingModel:
+    """Index map of a modular ring cache of exactly W rows ([BONSAI] Steps 1-3:
+    a smaller cache for the local layers, positions assigned with ``%`` and
+    wrapping around, and a window mask compatible with the wrap).
+
+    Readings where the page is silent:
+      * the ring has W rows and position pos lives in row pos % W, so writing
+        position p overwrites position p - W, the first one outside the window;
+      * the prompt's last W positions are copied in at first decode (from the
+        prompt-sized prefill cache), each to its own row pos % W;
+      * a row is admitted when the position it holds lies in (p - W, p] and at
+        or after the sequence's first valid position; no roll ever happens.
+    """
+
+    def __init__(self, prompt_len: int, window: int):
+        self.S = int(prompt_len)
+        self.W = int(window)
+        self.R = self.W
+        self.step = 0
+        self.cur_row = -1
+        self.held = np.full(self.R, -1, dtype=np.int64)
+        for pos in range(max(0, self.S - self.W), self.S):
+            self.held[pos % self.W] = pos
+
+    def needs_roll(self) -> bool:
+        return False
+
+    def begin_step(self, valid_start) -> np.ndarray:
+        """Advance one decode step; return the runtime mask [B, W] (bool).
+
+        The step's key/value is written to row p % W first; then a row is
+        admitted when the position it holds is written, lies in (p - W, p] and
+        is >= valid_start[b].
+        """
+        vs = np.asarray(valid_start, dtype=np.int64).reshape(-1)
+        p = self.S + self.step
+        cur = p % self.W
+        self.held[cur] = p
+        pos = self.held
+        ok = (pos >= 0) & (pos > p - self.W) & (pos <= p)
+        mask = ok[None, :] & (pos[None, :] >= vs[:, None])
+        self.cur_row = cur
+        self.step += 1
+        return mask
+
+    def query_position(self) -> int:
+        return self.S + self.step - 1
+
+    def expected_cache(self, full: np.ndarray, first_pos: int = 0) -> np.ndarray:
+        """Contents of the ring gathered from a full-length array (``full[i]``
+        holds position ``first_pos + i``), zeros for rows never written."""
+        out = np.zeros((self.R,) + full.shape[1:], dtype=full.dtype)
+        ok = self.held >= 0
+        idx = self.held[ok] - first_pos
+        if (idx < 0).any() or (idx >= full.shape[0]).any():
+            raise ValueError("the cache holds positions outside the given array")
+        out[ok] = full[idx]
+        return out

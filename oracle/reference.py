@@ -23,7 +23,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import attention, masks
-from .compact import CompactModel
+from .compact import CompactModel, RingModel
 
 
 def _f64(x) -> np.ndarray:
@@ -96,8 +96,9 @@ def decode_full(prompt_k, prompt_v, dec_q, dec_k, dec_v, prompt_len: int, window
 
 
 def decode_compact(prompt_k, prompt_v, dec_q, dec_k, dec_v, prompt_len: int, window: int,
-                   scale: float, valid_start=None, on_step=None):
-    """The same decode loop through the compact cache model.
+                   scale: float, valid_start=None, on_step=None, ring: bool = False):
+    """The same decode loop through the compact cache model (or, with
+    ``ring``, through the modular ring model).
 
     The compact cache of each sequence is materialised from the model's
     row -> position map; the runtime mask comes from the model.  ``on_step``
@@ -109,7 +110,7 @@ def decode_compact(prompt_k, prompt_v, dec_q, dec_k, dec_v, prompt_len: int, win
     p_rows = pk.shape[1]
     start = prompt_len - p_rows
     vs = np.zeros(b_count, dtype=np.int64) if valid_start is None else np.asarray(valid_start)
-    model = CompactModel(prompt_len, window)
+    model = RingModel(prompt_len, window) if ring else CompactModel(prompt_len, window)
     o = np.zeros(dq.shape, dtype=np.float64)
     lse = np.full(dq.shape[:3], -np.inf, dtype=np.float64)
     for t in range(t_count):

@@ -9,7 +9,11 @@
   single-stream shape;
 * pad rows and never-written rows get zero weight (bit-identical outputs
   after filling them with large finite values);
-* rolls happen exactly every 64 decode steps whatever the prompt length.
+* rolls happen exactly every 64 decode steps whatever the prompt length;
+* the modular ring (W rows, position p in row p % W) admits the same
+  positions as the full-length predicate at every step, never rolls, and its
+  decode equals the full-cache decode up to fp64 rounding (its rows come in a
+  different order, so the sums differ in their last bits only).
 """
 
 import json
@@ -19,7 +23,7 @@ import numpy as np
 import pytest
 
 from oracle import masks, reference
-from oracle.compact import CompactModel
+from oracle.compact import CompactModel, RingModel
 from sliding_window_gqa_swa_gb300 import synth
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "index_map_s200_w64.json")
@@ -140,3 +144,44 @@ def test_roll_requires_full_cache():
         m.begin_step([0])
     m.roll()
     assert m.origin == 100 and m.next_row == 64
+
+
+@pytest.mark.parametrize("prompt_len,window,vs", [(200, 64, 0), (200, 64, 150), (40, 64, 0), (40, 64, 7),
+                                                   (1000, 128, 900), (129, 128, 3), (64, 64, 0), (5, 3, 1)])
+def test_ring_mask_admits_exactly_the_window(prompt_len, window, vs):
+    m = RingModel(prompt_len, window)
+    for t in range(300):
+        assert not m.needs_roll()
+        mask = m.begin_step([vs])[0]
+        p = m.query_position()
+        got = sorted(m.held[mask].tolist())
+        pos = np.arange(0, p + 1)
+        exp = pos[masks.decode_mask_full(p, window, vs, pos)].tolist()
+        assert got == exp, (t, got[:5], exp[:5])
+        # every written row holds a position congruent to its index, the
+        # current one in row p % W
+        w = m.held >= 0
+        assert np.all(m.held[w] % window == np.flatnonzero(w))
+        assert m.cur_row == p % window and m.held[m.cur_row] == p
+
+
+def test_ring_equals_full_with_padding_and_short_prompt():
+    c = synth.decode_case(78, batch=3, q_heads=4, kv_heads=2, head_dim=16, window=64, prompt_len=40,
+                          steps=150, layers=1)
+    vs = np.array([0, 5, 39])
+    args = (c.prompt_k[0], c.prompt_v[0], c.dec_q[:, 0], c.dec_k[:, 0], c.dec_v[:, 0], c.prompt_len,
+            c.window, 0.25, vs)
+    o_full, l_full = reference.decode_full(*args)
+    o_ring, l_ring = reference.decode_compact(*args, ring=True)
+    assert np.allclose(o_ring, o_full, rtol=1e-12, atol=1e-12)
+    assert np.allclose(l_ring, l_full, rtol=1e-12, atol=1e-12)
+
+
+def test_ring_equals_full_70_steps():
+    c = synth.workload1()
+    args = (c.prompt_k[0], c.prompt_v[0], c.dec_q[:, 0], c.dec_k[:, 0], c.dec_v[:, 0], c.prompt_len,
+            c.window, c.head_dim ** -0.5, c.valid_start)
+    o_full, l_full = reference.decode_full(*args)
+    o_ring, l_ring = reference.decode_compact(*args, ring=True)
+    assert np.allclose(o_ring, o_full, rtol=1e-12, atol=1e-12)
+    assert np.allclose(l_ring, l_full, rtol=1e-12, atol=1e-12)
