@@ -66,7 +66,7 @@ typedef enum swa_status {
   SWA_EDEVICE = 6       /* an earlier kernel recorded a device-side error */
 } swa_status;
 
-enum { SWA_CACHE_PREFILL = 0, SWA_CACHE_COMPACT = 1 };
+enum { SWA_CACHE_PREFILL = 0, SWA_CACHE_COMPACT = 1, SWA_CACHE_RING = 2 };
 enum { SWA_MODE_CAUSAL = 0, SWA_MODE_GENERIC = 1 };
 enum { SWA_MASK_DECODE = 0, SWA_MASK_PREFILL = 1, SWA_MASK_DENSE_DEBUG = 2 };
 
@@ -84,10 +84,15 @@ enum { SWA_MASK_DECODE = 0, SWA_MASK_PREFILL = 1, SWA_MASK_DENSE_DEBUG = 2 };
  *   kind       SWA_CACHE_PREFILL: prompt-sized, row = position ([SPYRE]
  *              Summary: prompt-sized sliding caches).
  *              SWA_CACHE_COMPACT: W + 64 rows, row r holds position origin + r.
+ *              SWA_CACHE_RING: W rows, position p lives in row p % W; it never
+ *              rolls ([BONSAI] Steps 1-3: smaller caches for the local layers,
+ *              positions assigned with % and wrapping around, a window mask
+ *              compatible with the wrap).  Decodes like a compact cache.
  *   prompt_len S, the padded prompt length (positions 0 .. S-1).
  *   rows       0 selects the default: max(S, W + 64) for a prefill cache
  *              (short prompts still get the minimum width, [SPYRE] Summary),
- *              W + 64 for a compact cache (the only value accepted there).
+ *              W + 64 for a compact cache, W for a ring (the only values
+ *              accepted there).
  *   window     W >= 1; a compact cache needs W >= 64. */
 typedef struct swa_cache_desc {
   int32_t kind;
@@ -125,7 +130,8 @@ SWA_API size_t swa_cache_bytes(const swa_cache_desc* desc);
  * 256-byte aligned), zero-fill it and write the initial state:
  *   prefill cache: origin 0, next_row S;   compact cache: origin S - W,
  *   next_row W (right-aligned anchoring; rows of negative positions stay
- *   zero and are never admitted by the mask).
+ *   zero and are never admitted by the mask);   ring: origin 0 (unused),
+ *   next_row S % W.
  * dev_valid_start: [batch] int32 device array of left-pad counts (copied),
  * or NULL for no padding.  On success *out receives a handle the caller frees
  * with swa_cache_free (which never frees dev_mem). */
@@ -199,6 +205,10 @@ SWA_API size_t swa_prefill_plan_bytes(const swa_prefill_meta* meta);
  *   and mask[b, r] = (r <= cur_row) and (pos_r > p - W) and
  *   (pos_r >= valid_start[b]) and (pos_r >= 0), pos_r = origin + r,
  *   p = S + step (before the increment).  SWA_ESTATE when a roll is due.
+ *   Ring cache (SWA_MASK_DECODE on SWA_CACHE_RING): cur_row = p % W,
+ *   next_row = (p + 1) % W, and mask[b, r] = (pos_r >= valid_start[b]) and
+ *   (pos_r >= 0) with pos_r = p - ((p - r) mod W), the position row r holds
+ *   (always in (p - W, p]).
  * SWA_MASK_PREFILL (cache may be NULL, meta required): the prefill plan at
  *   dev_out (swa_prefill_plan_bytes): for every query row the interval
  *   [lo, hi] of keys it attends (the predicate above reduces to one interval
@@ -241,7 +251,8 @@ SWA_API swa_status swa_prefill(swa_cache* cache, int32_t layer, int32_t mode, in
 /* Compaction at first decode ([SPYRE] Summary): rows [S - W, S) of every
  * (layer, sequence, head) slab of the prefill cache go to rows [0, W) of the
  * compact cache (same shape apart from rows, same S and W); rows of negative
- * positions are zero.  Bit-exact copy. */
+ * positions are zero.  Into a ring cache, position pos goes to row pos % W
+ * instead.  Bit-exact copy. */
 SWA_API swa_status swa_compact(const swa_cache* prefill, swa_cache* compact, swa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -303,7 +314,8 @@ SWA_API swa_status swa_decode_noalloc(swa_cache* cache, int32_t layer, int32_t q
 /* The roll every 64 decode tokens ([SPYRE] Summary: offset-aware
  * device-to-device copies): when next_row == rows, rows [64, rows) of every
  * slab of every layer move to rows [0, W) (an overlap-safe in-place shift),
- * origin += 64, next_row = W.  SWA_ESTATE unless the roll is due. */
+ * origin += 64, next_row = W.  SWA_ESTATE unless the roll is due (a ring
+ * cache never rolls). */
 SWA_API swa_status swa_roll(swa_cache* cache, swa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */

@@ -54,14 +54,17 @@ struct Layout {
 };
 
 // Validate a desc and resolve rows; returns false with g_error set.
+// Caches that decode: the anchored compact buffer and the modular ring.
+bool decodes(int32_t kind) { return kind == SWA_CACHE_COMPACT || kind == SWA_CACHE_RING; }
+
 bool resolve_desc(const swa_cache_desc* in, swa_cache_desc* out) {
   if (!in) {
     fail(SWA_EINVAL, "desc is NULL");
     return false;
   }
   swa_cache_desc d = *in;
-  if (d.kind != SWA_CACHE_PREFILL && d.kind != SWA_CACHE_COMPACT) {
-    fail(SWA_EINVAL, "desc.kind must be SWA_CACHE_PREFILL or SWA_CACHE_COMPACT");
+  if (d.kind != SWA_CACHE_PREFILL && d.kind != SWA_CACHE_COMPACT && d.kind != SWA_CACHE_RING) {
+    fail(SWA_EINVAL, "desc.kind must be SWA_CACHE_PREFILL, SWA_CACHE_COMPACT or SWA_CACHE_RING");
     return false;
   }
   if (d.layers < 1 || d.batch < 1 || d.kv_heads < 1) {
@@ -87,6 +90,12 @@ bool resolve_desc(const swa_cache_desc* in, swa_cache_desc* out) {
       return false;
     }
     d.rows = want;
+  } else if (d.kind == SWA_CACHE_RING) {
+    if (d.rows != 0 && d.rows != d.window) {
+      fail(SWA_EINVAL, "a ring cache has exactly window rows");
+      return false;
+    }
+    d.rows = d.window;
   } else {
     const int64_t minr = std::max<int64_t>(d.prompt_len, int64_t(d.window) + SWA_ROLL_ROWS);
     if (d.rows == 0) d.rows = int32_t(std::min<int64_t>(minr, INT32_MAX));
@@ -208,6 +217,9 @@ swa_status swa_cache_alloc(const swa_cache_desc* desc, void* dev_mem, size_t byt
   if (d.kind == SWA_CACHE_COMPACT) {
     init.origin = d.prompt_len - d.window;
     init.next_row = d.window;
+  } else if (d.kind == SWA_CACHE_RING) {
+    init.origin = 0;
+    init.next_row = d.prompt_len % d.window;
   } else {
     init.origin = 0;
     init.next_row = d.prompt_len;
@@ -259,9 +271,16 @@ swa_status swa_cache_position(const swa_cache* c, int32_t* origin, int32_t* next
 
 swa_status swa_cache_advance(swa_cache* c, int32_t steps) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
-  if (c->desc.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "only a compact cache decodes");
+  if (!decodes(c->desc.kind)) return fail(SWA_ESTATE, "only a compact or ring cache decodes");
   if (steps < 0) return fail(SWA_EINVAL, "steps must be >= 0");
   if (steps == 0) return SWA_OK;
+  if (c->desc.kind == SWA_CACHE_RING) {  // never rolls
+    const int32_t R = c->desc.rows;
+    c->cur_row = int32_t((int64_t(c->next_row) + steps - 1) % R);
+    c->next_row = int32_t((int64_t(c->next_row) + steps) % R);
+    c->step += steps;
+    return SWA_OK;
+  }
   if (int64_t(c->next_row) + steps > c->desc.rows)
     return fail(SWA_ESTATE, "advancing %d steps runs past a due roll (next_row = %d, rows = %d)", steps,
                 c->next_row, c->desc.rows);
@@ -316,15 +335,16 @@ swa_status swa_build_mask(swa_cache* c, int32_t kind, const swa_prefill_meta* me
   if (!dev_out) return fail(SWA_EINVAL, "dev_out is NULL");
   if (kind == SWA_MASK_DECODE) {
     if (!c) return fail(SWA_EINVAL, "a decode mask needs a cache");
-    if (c->desc.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "a decode mask needs a compact cache");
+    if (!decodes(c->desc.kind)) return fail(SWA_ESTATE, "a decode mask needs a compact or ring cache");
     if (meta) return fail(SWA_EINVAL, "a decode mask takes no prefill meta");
-    if (c->next_row >= c->desc.rows)
+    const bool ring = c->desc.kind == SWA_CACHE_RING;
+    if (!ring && c->next_row >= c->desc.rows)
       return fail(SWA_ESTATE, "a roll is due before the next decode step (next_row == rows)");
-    cudaError_t e = swa::launch_decode_mask(c->state, c->valid_start, c->desc.batch, c->desc.rows,
+    cudaError_t e = swa::launch_decode_mask(c->state, c->valid_start, c->desc.batch, c->desc.rows, ring,
                                             static_cast<uint8_t*>(dev_out), stream);
     if (e != cudaSuccess) return cuda_fail(e, "decode mask launch");
     c->cur_row = c->next_row;
-    c->next_row += 1;
+    c->next_row = (ring && c->next_row + 1 == c->desc.rows) ? 0 : c->next_row + 1;
     c->step += 1;
     return SWA_OK;
   }
@@ -422,8 +442,8 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
 
 swa_status swa_compact(const swa_cache* p, swa_cache* c, swa_stream_t stream) {
   if (!p || !c) return fail(SWA_EINVAL, "cache is NULL");
-  if (p->desc.kind != SWA_CACHE_PREFILL || c->desc.kind != SWA_CACHE_COMPACT)
-    return fail(SWA_ESTATE, "compaction goes from a prefill cache to a compact cache");
+  if (p->desc.kind != SWA_CACHE_PREFILL || !decodes(c->desc.kind))
+    return fail(SWA_ESTATE, "compaction goes from a prefill cache to a compact or ring cache");
   const swa_cache_desc &a = p->desc, &b = c->desc;
   if (a.layers != b.layers || a.batch != b.batch || a.kv_heads != b.kv_heads || a.head_dim != b.head_dim ||
       a.window != b.window || a.prompt_len != b.prompt_len)
@@ -431,7 +451,7 @@ swa_status swa_compact(const swa_cache* p, swa_cache* c, swa_stream_t stream) {
   if (c->step != 0) return fail(SWA_ESTATE, "the compact cache has already been decoded into");
   const long long slabs = (long long)a.layers * a.batch * a.kv_heads;
   cudaError_t e = swa::launch_compact(c->k, c->v, p->k, p->v, slabs, a.rows, b.rows, b.window,
-                                      b.prompt_len, b.head_dim, stream);
+                                      b.prompt_len, b.head_dim, b.kind == SWA_CACHE_RING, stream);
   if (e != cudaSuccess) return cuda_fail(e, "compact launch");
   return SWA_OK;
 }
@@ -455,7 +475,7 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
                       swa_bf16* out, float* lse, void* workspace, size_t ws_bytes, swa_stream_t stream) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
   const swa_cache_desc& d = c->desc;
-  if (d.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "decode needs a compact cache");
+  if (!decodes(d.kind)) return fail(SWA_ESTATE, "decode needs a compact or ring cache");
   if (layer < 0 || layer >= d.layers) return fail(SWA_EINVAL, "layer %d out of range", layer);
   if (q_heads < 1 || q_heads % d.kv_heads) return fail(SWA_EINVAL, "q_heads must be a positive multiple of kv_heads");
   const int g = q_heads / d.kv_heads;
@@ -508,7 +528,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
                               swa_bf16* out, float* lse, swa_stream_t stream) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
   const swa_cache_desc& d = c->desc;
-  if (d.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "decode needs a compact cache");
+  if (!decodes(d.kind)) return fail(SWA_ESTATE, "decode needs a compact or ring cache");
   if (layer < 0 || layer >= d.layers) return fail(SWA_EINVAL, "layer %d out of range", layer);
   if (q_heads < 1 || q_heads % d.kv_heads) return fail(SWA_EINVAL, "q_heads must be a positive multiple of kv_heads");
   const int g = q_heads / d.kv_heads;
@@ -566,6 +586,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
 swa_status swa_roll(swa_cache* c, swa_stream_t stream) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
   const swa_cache_desc& d = c->desc;
+  if (d.kind == SWA_CACHE_RING) return fail(SWA_ESTATE, "a ring cache never rolls");
   if (d.kind != SWA_CACHE_COMPACT) return fail(SWA_ESTATE, "only a compact cache rolls");
   if (c->next_row != d.rows)
     return fail(SWA_ESTATE, "a roll is due only when next_row == rows (next_row = %d)", c->next_row);

@@ -44,7 +44,7 @@ __global__ void write_rows_kernel(uint4* __restrict__ ck, uint4* __restrict__ cv
 __global__ void compact_kernel(uint4* __restrict__ dk, uint4* __restrict__ dv,
                                const uint4* __restrict__ sk, const uint4* __restrict__ sv,
                                long long slabs, int src_rows, int dst_rows, int window,
-                               int prompt_len, int d8) {
+                               int prompt_len, int d8, int ring) {
   const long long n = slabs * window * d8;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -59,7 +59,8 @@ __global__ void compact_kernel(uint4* __restrict__ dk, uint4* __restrict__ dv,
       a = sk[src];
       b = sv[src];
     }
-    const long long dst = (slab * dst_rows + r) * d8 + c;
+    const int dr = ring ? ((pos % window) + window) % window : r;  // ring: row pos % W
+    const long long dst = (slab * dst_rows + dr) * d8 + c;
     dk[dst] = a;
     dv[dst] = b;
   }
@@ -135,14 +136,14 @@ cudaError_t launch_write_rows(uint16_t* cache_k, uint16_t* cache_v, const uint16
 
 cudaError_t launch_compact(uint16_t* dk, uint16_t* dv, const uint16_t* sk, const uint16_t* sv,
                            long long slabs, int src_rows, int dst_rows, int window,
-                           int prompt_len, int head_dim, cudaStream_t s) {
+                           int prompt_len, int head_dim, bool ring, cudaStream_t s) {
   const int d8 = head_dim / 8;
   const long long n = slabs * window * d8;
   if (n == 0) return cudaSuccess;
   compact_kernel<<<grid_for(n, 256), 256, 0, s>>>(
       reinterpret_cast<uint4*>(dk), reinterpret_cast<uint4*>(dv),
       reinterpret_cast<const uint4*>(sk), reinterpret_cast<const uint4*>(sv), slabs, src_rows,
-      dst_rows, window, prompt_len, d8);
+      dst_rows, window, prompt_len, d8, ring ? 1 : 0);
   return cudaGetLastError();
 }
 

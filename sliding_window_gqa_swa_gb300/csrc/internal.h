@@ -78,14 +78,15 @@ cudaError_t launch_write_rows(uint16_t* cache_k, uint16_t* cache_v, const uint16
                               const uint16_t* v, int batch, int chunk_len, int kv_heads,
                               int head_dim, int rows, int layer, int chunk_start, cudaStream_t s);
 
+// ring: position pos goes to row pos % window instead of row pos - (S - W)
 cudaError_t launch_compact(uint16_t* dk, uint16_t* dv, const uint16_t* sk, const uint16_t* sv,
                            long long slabs, int src_rows, int dst_rows, int window,
-                           int prompt_len, int head_dim, cudaStream_t s);
+                           int prompt_len, int head_dim, bool ring, cudaStream_t s);
 
 cudaError_t launch_roll(uint16_t* k, uint16_t* v, long long slabs, int rows, int window,
                         int head_dim, swa_device_state* st, cudaStream_t s);
 
-cudaError_t launch_decode_mask(swa_device_state* st, const int32_t* vs, int batch, int rows,
+cudaError_t launch_decode_mask(swa_device_state* st, const int32_t* vs, int batch, int rows, bool ring,
                                uint8_t* mask, cudaStream_t s);
 
 cudaError_t launch_prefill_plan(const swa_prefill_meta& meta, void* plan, cudaStream_t s);

@@ -16,16 +16,24 @@ namespace {
 
 constexpr int kMaskThreads = 512;
 
+// Position held by row r: anchored (origin + r), or in a ring of `rows` rows
+// the latest position congruent to r that is <= p ("Gemma3 Local Attention
+// Cache", Steps 2-3: positions assigned with % and wrapping around).
+__device__ __forceinline__ int row_position(int r, int origin, int p, int rows, bool ring) {
+  return ring ? p - (((p - r) % rows) + rows) % rows : origin + r;
+}
+
 // Decode mask of the step about to run (one block).  Every thread reads the
 // state first; thread 0 advances it after a barrier.
 __global__ void __launch_bounds__(kMaskThreads)
-decode_mask_kernel(swa_device_state* st, const int32_t* __restrict__ vs, int batch, int rows,
+decode_mask_kernel(swa_device_state* st, const int32_t* __restrict__ vs, int batch, int rows, int ring,
                    uint8_t* __restrict__ mask) {
   const int origin = st->origin;
   const int cur = st->next_row;
   const int p = st->prompt_len + st->step;
   const int window = st->window;
-  const bool ok = cur >= 0 && cur < rows;
+  // a ring writes position p to row p % rows; an anchored cache never past its end
+  const bool ok = cur >= 0 && cur < rows && (!ring || cur == p % rows);
   const long long n = (long long)batch * rows;
   if ((rows & 15) == 0 && (reinterpret_cast<uintptr_t>(mask) & 15) == 0) {
     // 16 rows per thread-iteration, written as one 16-byte store
@@ -41,8 +49,8 @@ decode_mask_kernel(swa_device_state* st, const int32_t* __restrict__ vs, int bat
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int r = r0 + j * 4 + e;
-          const int pos = origin + r;
-          const bool m = ok && r <= cur && pos > p - window && pos >= v && pos >= 0;
+          const int pos = row_position(r, origin, p, rows, ring);
+          const bool m = ok && (ring || r <= cur) && pos > p - window && pos >= v && pos >= 0;
           x |= uint32_t(m) << (8 * e);
         }
         w[j] = x;
@@ -53,18 +61,18 @@ decode_mask_kernel(swa_device_state* st, const int32_t* __restrict__ vs, int bat
     for (long long i = threadIdx.x; i < n; i += blockDim.x) {
       const int b = int(i / rows);
       const int r = int(i % rows);
-      const int pos = origin + r;
-      mask[i] = uint8_t(ok && r <= cur && pos > p - window && pos >= vs[b] && pos >= 0);
+      const int pos = row_position(r, origin, p, rows, ring);
+      mask[i] = uint8_t(ok && (ring || r <= cur) && pos > p - window && pos >= vs[b] && pos >= 0);
     }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     if (ok) {
       st->cur_row = cur;
-      st->next_row = cur + 1;
+      st->next_row = (ring && cur + 1 == rows) ? 0 : cur + 1;
       st->step = st->step + 1;
     } else {
-      atomicCAS(&st->error, 0, kErrRollDue);
+      atomicCAS(&st->error, 0, ring ? kErrRowRange : kErrRollDue);
     }
   }
 }
@@ -233,9 +241,9 @@ __global__ void dense_debug_kernel(swa_prefill_meta meta, uint8_t* __restrict__ 
 
 }  // namespace
 
-cudaError_t launch_decode_mask(swa_device_state* st, const int32_t* vs, int batch, int rows,
+cudaError_t launch_decode_mask(swa_device_state* st, const int32_t* vs, int batch, int rows, bool ring,
                                uint8_t* mask, cudaStream_t s) {
-  decode_mask_kernel<<<1, kMaskThreads, 0, s>>>(st, vs, batch, rows, mask);
+  decode_mask_kernel<<<1, kMaskThreads, 0, s>>>(st, vs, batch, rows, ring ? 1 : 0, mask);
   return cudaGetLastError();
 }
 

@@ -25,7 +25,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 # status codes and enums (include/swa.h)
 OK, EINVAL, ESTATE, EUNSUPPORTED, ECUDA, ETIMEOUT, EDEVICE = range(7)
-CACHE_PREFILL, CACHE_COMPACT = 0, 1
+CACHE_PREFILL, CACHE_COMPACT, CACHE_RING = 0, 1, 2
 MODE_CAUSAL, MODE_GENERIC = 0, 1
 MASK_DECODE, MASK_PREFILL, MASK_DENSE_DEBUG = 0, 1, 2
 ROLL_ROWS = 64
@@ -176,7 +176,8 @@ class Cache:
         return o.value, n.value, s.value
 
     def needs_roll(self) -> bool:
-        return self.position()[1] == self.rows
+        # a ring cache never rolls
+        return self.desc.kind == CACHE_COMPACT and self.position()[1] == self.rows
 
     def advance(self, steps: int = 1) -> None:
         """Advance the host mirror for steps replayed from a captured graph."""

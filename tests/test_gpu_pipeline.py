@@ -11,6 +11,8 @@ through the C ABI, against the fp64 oracle:
   * every decode output and lse against the full-length oracle decode;
   * one captured CUDA graph (mask + decode) replayed across positions gives
     the eager results (the pages' graph-reuse observation).
+The same checks run through the modular ring cache (W rows, position p in
+row p % W, no roll) against the oracle's RingModel.
 """
 
 import numpy as np
@@ -18,7 +20,7 @@ import pytest
 import torch
 
 from oracle import reference
-from oracle.compact import CompactModel
+from oracle.compact import CompactModel, RingModel
 from sliding_window_gqa_swa_gb300 import synth
 from tests._gpu import assert_close, assert_lse, bits
 
@@ -40,7 +42,7 @@ def _full_kv(c, b, t_count):
     return k, v
 
 
-def run_decode_case(swa, c, check_every_step=True):
+def run_decode_case(swa, c, check_every_step=True, ring=False):
     dev = torch.device("cuda")
     S, W, D = c.prompt_len, c.window, c.head_dim
     B, Hq, Hkv = c.batch, c.q_heads, c.kv_heads
@@ -49,7 +51,7 @@ def run_decode_case(swa, c, check_every_step=True):
     vs = c.valid_start.to(dev)
 
     out = lse = None
-    cmp_ = swa.Cache(swa.CACHE_COMPACT, 1, B, Hkv, D, W, S, vs)
+    cmp_ = swa.Cache(swa.CACHE_RING if ring else swa.CACHE_COMPACT, 1, B, Hkv, D, W, S, vs)
     if D in (256, 512):
         # the whole path: prefill into the prompt-sized cache, then compaction
         pre = swa.Cache(swa.CACHE_PREFILL, 1, B, Hkv, D, W, S, vs)
@@ -66,11 +68,17 @@ def run_decode_case(swa, c, check_every_step=True):
         swa.compact(pre, cmp_)
     else:
         # prefill supports D = 256 / 512 only: place the prompt's last W positions
-        # in rows [max(0, W - S), W) as compaction would (decode-only head sizes)
+        # as compaction would (decode-only head sizes): anchored rows
+        # [max(0, W - S), W), or ring rows pos % W
         n = min(S, W)
-        cmp_.k[0, :, :, W - n:W] = c.prompt_k[0, :, S - n:].transpose(1, 2).to(dev)
-        cmp_.v[0, :, :, W - n:W] = c.prompt_v[0, :, S - n:].transpose(1, 2).to(dev)
-    model = CompactModel(S, W)
+        if ring:
+            for pos in range(S - n, S):
+                cmp_.k[0, :, :, pos % W] = c.prompt_k[0, :, pos].to(dev)
+                cmp_.v[0, :, :, pos % W] = c.prompt_v[0, :, pos].to(dev)
+        else:
+            cmp_.k[0, :, :, W - n:W] = c.prompt_k[0, :, S - n:].transpose(1, 2).to(dev)
+            cmp_.v[0, :, :, W - n:W] = c.prompt_v[0, :, S - n:].transpose(1, 2).to(dev)
+    model = RingModel(S, W) if ring else CompactModel(S, W)
     torch.cuda.synchronize()
     for b in range(B):
         fk, _ = _full_kv(c, b, 0)
@@ -99,8 +107,11 @@ def run_decode_case(swa, c, check_every_step=True):
             torch.cuda.synchronize()
             assert np.array_equal(mask.cpu().numpy().astype(bool), mexp), f"mask differs at step {t}"
             st = cmp_.state()
-            assert (st["origin"], st["next_row"], st["cur_row"], st["step"], st["error"]) == \
-                (model.origin, model.next_row, model.cur_row, model.step, 0), (t, st)
+            if ring:
+                exp_st = (0, (S + model.step) % W, model.cur_row, model.step, 0)
+            else:
+                exp_st = (model.origin, model.next_row, model.cur_row, model.step, 0)
+            assert (st["origin"], st["next_row"], st["cur_row"], st["step"], st["error"]) == exp_st, (t, st)
             for b in range(B):
                 fk, fv = _full_kv(c, b, t + 1)
                 ek = torch.from_numpy(model.expected_cache(fk)).to(torch.bfloat16)
@@ -142,7 +153,45 @@ def test_decode_shapes_with_padding(swa, batch, hq, hkv, d, w, s):
     assert_lse(dec_l, ref_l, "decode lse")
 
 
-def test_graph_replay_matches_eager(swa):
+def test_workload1_ring(swa):
+    c = synth.workload1()
+    _, _, dec_o, dec_l, ref_o, ref_l = run_decode_case(swa, c, ring=True)
+    assert_close(dec_o, ref_o, "ring decode")
+    assert_lse(dec_l, ref_l, "ring decode lse")
+
+
+@pytest.mark.parametrize("batch,hq,hkv,d,w,s", [(3, 4, 2, 256, 64, 40), (2, 8, 2, 128, 64, 300),
+                                                (1, 4, 2, 256, 1024, 1500)])
+def test_ring_decode_shapes_with_padding(swa, batch, hq, hkv, d, w, s):
+    c = synth.decode_case(3300 + d + hq, batch=batch, q_heads=hq, kv_heads=hkv, head_dim=d, window=w,
+                          prompt_len=s, steps=140, layers=1, with_prompt_q=False)
+    vs = torch.tensor([0, min(s - 1, 13), 5][:batch], dtype=torch.int32)
+    c.valid_start = vs
+    for b in range(batch):
+        c.prompt_k[0, b, :int(vs[b])] = 50.0
+        c.prompt_v[0, b, :int(vs[b])] = -70.0
+    _, _, dec_o, dec_l, ref_o, ref_l = run_decode_case(swa, c, check_every_step=False, ring=True)
+    assert_close(dec_o, ref_o, "ring decode")
+    assert_lse(dec_l, ref_l, "ring decode lse")
+
+
+def test_ring_never_rolls(swa):
+    dev = torch.device("cuda")
+    cache = swa.Cache(swa.CACHE_RING, 1, 1, 2, 256, 64, 100)
+    assert cache.rows == 64 and not cache.needs_roll()
+    mask = torch.empty(1, 64, dtype=torch.uint8, device=dev)
+    for _ in range(130):
+        swa.build_decode_mask(cache, mask)
+    assert not cache.needs_roll()
+    with pytest.raises(swa.SwaError):
+        swa.roll(cache)
+    torch.cuda.synchronize()
+    st = cache.state()
+    assert (st["next_row"], st["cur_row"], st["step"], st["error"]) == ((100 + 130) % 64, (100 + 129) % 64, 130, 0)
+
+
+@pytest.mark.parametrize("ring", [False, True])
+def test_graph_replay_matches_eager(swa, ring):
     """One captured graph (mask + decode) serves every position between rolls."""
     dev = torch.device("cuda")
     c = synth.decode_case(3200, batch=2, q_heads=4, kv_heads=2, head_dim=256, window=64, prompt_len=150,
@@ -155,7 +204,7 @@ def test_graph_replay_matches_eager(swa):
         swa.prefill(pre, 0, swa.MODE_CAUSAL, torch.zeros(B, S, Hq, D, dtype=torch.bfloat16, device=dev),
                     c.prompt_k[0].to(dev), c.prompt_v[0].to(dev), swa.Meta(B, S, 0, S, W), scale,
                     torch.empty(B, S, Hq, D, dtype=torch.bfloat16, device=dev))
-        cache = swa.Cache(swa.CACHE_COMPACT, 1, B, Hkv, D, W, S)
+        cache = swa.Cache(swa.CACHE_RING if ring else swa.CACHE_COMPACT, 1, B, Hkv, D, W, S)
         swa.compact(pre, cache)
         mask = torch.empty(B, cache.rows, dtype=torch.uint8, device=dev)
         ws = swa.decode_workspace(cache, Hq)
