@@ -153,7 +153,7 @@ def ev():
 class SingleStreamJob:
     """The whole single-stream job on one GPU (one bench step)."""
 
-    def __init__(self, swa, case, dev, e2e=False):
+    def __init__(self, swa, case, dev, e2e=False, ring=False):
         self.swa, self.dev, self.e2e = swa, dev, e2e
         c = case
         self.L, self.S, self.W, self.D = c.layers, c.prompt_len, c.window, c.head_dim
@@ -172,7 +172,9 @@ class SingleStreamJob:
             self.outs = torch.empty((self.T, self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
         self.prefill_out = torch.empty((self.B, self.S, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
         self.pre = swa.Cache(swa.CACHE_PREFILL, self.L, self.B, self.Hkv, self.D, self.W, self.S)
-        self.cmp = swa.Cache(swa.CACHE_COMPACT, self.L, self.B, self.Hkv, self.D, self.W, self.S)
+        # the anchored W + 64 buffer with a roll every 64 steps, or the modular ring of W rows
+        self.cmp = swa.Cache(swa.CACHE_RING if ring else swa.CACHE_COMPACT, self.L, self.B, self.Hkv, self.D,
+                             self.W, self.S)
         self.meta = swa.Meta(self.B, self.S, 0, self.S, self.W)
         self.mask = torch.empty(self.B, self.cmp.rows, dtype=torch.uint8, device=dev)
         self.ws = swa.decode_workspace(self.cmp, self.Hq)
@@ -182,7 +184,7 @@ class SingleStreamJob:
         self.vb = torch.empty_like(self.kb)
         self.ob = torch.empty((self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
         self.graph = None
-        self.rolls = (self.T - 1) // 64
+        self.rolls = 0 if ring else (self.T - 1) // 64
         # kernels of ours per job: 2 cache bindings, (K/V write + attention) per layer, compaction,
         # (mask + one decode per layer) per step, rolls
         self.launches = 2 + 2 * self.L + 1 + self.T * (1 + self.L) + self.rolls
@@ -320,6 +322,26 @@ def run_ours(args):
         torch.cuda.empty_cache()
 
     secondary = {} if args.no_secondary else run_secondary(swa, synth, dev, peaks)
+    if not args.no_secondary:
+        # the same job through the modular ring cache (W rows, no roll)
+        rjob = SingleStreamJob(swa, case, dev, ring=True)
+        for _ in range(max(1, min(args.warmup, 2))):
+            rjob.run(rjob.make_events())
+        torch.cuda.synchronize()
+        rev = [rjob.make_events() for _ in range(args.steps)]
+        for k in range(args.steps):
+            rjob.run(rev[k])
+        torch.cuda.synchronize()
+        r_dec = sum(e["decode_start"].elapsed_time(e["end"]) for e in rev)
+        r_graph = sum(sum(e["step_s"][t].elapsed_time(e["step_e"][t]) for t in range(T)) for e in rev)
+        secondary["single_stream_ring"] = {
+            "workload": "the single-stream job with a modular ring cache of W rows (position p in row p % W, "
+                        "no roll) instead of the anchored W + 64 buffer",
+            "us_per_layer": round(r_dec * 1e3 / (args.steps * T * L), 4),
+            "decode_launch_us": round(r_graph * 1e3 / (args.steps * T * L), 4),
+            "anchored_us_per_layer": round(us_per_layer, 4)}
+        del rjob
+        torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case, args.cpu_seconds)
