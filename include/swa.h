@@ -272,6 +272,9 @@ SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_head
  * workspace: >= swa_decode_workspace_bytes device bytes, zero-filled before
  * its first use; each call leaves it ready for the next.  Calls that overlap
  * on the GPU need separate workspaces.
+ * KV-sharing layer ([SPYRE] Summary: KV-sharing behavior is preserved):
+ * k_new = v_new = NULL attends over layer `layer`'s rows without appending;
+ * that layer's own swa_decode must already have appended this step's row.
  * Launch chaining: the kernel is launched with programmatic dependent launch.
  * It may start while the previous kernel of the stream is still running and
  * read this layer's cache rows then; it waits for that kernel before reading
@@ -279,7 +282,8 @@ SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_head
  * So the kernel launched just before it on the stream must not write this
  * layer's cache rows (swa_build_mask, projections and the other layers'
  * swa_decode calls do not; swa_roll and swa_compact are followed by the
- * step's swa_build_mask anyway).
+ * step's swa_build_mask anyway).  A KV-sharing call reads nothing before
+ * that wait.
  * Supported: head_dim 64, 128, 256 or 512; Hq / Hkv in {1, 2, 4, 8}. */
 SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
                               const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,

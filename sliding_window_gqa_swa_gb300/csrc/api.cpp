@@ -482,9 +482,10 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   if (g != 1 && g != 2 && g != 4 && g != 8) return fail(SWA_EUNSUPPORTED, "decode supports Hq/Hkv in {1, 2, 4, 8}");
   if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256 && d.head_dim != 512)
     return fail(SWA_EUNSUPPORTED, "decode supports head_dim 64, 128, 256 and 512");
-  if (!q || !k_new || !v_new || !mask || !out || !workspace)
-    return fail(SWA_EINVAL, "q, k_new, v_new, mask, out and workspace are required");
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || !aligned16(workspace) ||
+  if (!q || !mask || !out || !workspace) return fail(SWA_EINVAL, "q, mask, out and workspace are required");
+  if (!k_new != !v_new) return fail(SWA_EINVAL, "k_new and v_new are both given or both NULL (KV-sharing layer)");
+  if (!aligned16(q) || (k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)) || !aligned16(out) ||
+      !aligned16(workspace) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
     return fail(SWA_EINVAL, "tensor pointers must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
@@ -535,8 +536,9 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   if (g != 1 && g != 2 && g != 4 && g != 8) return fail(SWA_EUNSUPPORTED, "decode supports Hq/Hkv in {1, 2, 4, 8}");
   if (d.head_dim != 64 && d.head_dim != 128 && d.head_dim != 256 && d.head_dim != 512)
     return fail(SWA_EUNSUPPORTED, "decode supports head_dim 64, 128, 256 and 512");
-  if (!q || !k_new || !v_new || !mask || !out) return fail(SWA_EINVAL, "q, k_new, v_new, mask and out are required");
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) ||
+  if (!q || !mask || !out) return fail(SWA_EINVAL, "q, mask and out are required");
+  if (!k_new != !v_new) return fail(SWA_EINVAL, "k_new and v_new are both given or both NULL (KV-sharing layer)");
+  if (!aligned16(q) || (k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)) || !aligned16(out) ||
       (lse && (reinterpret_cast<uintptr_t>(lse) & 3)))
     return fail(SWA_EINVAL, "tensor pointers must be 16-byte aligned");
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");

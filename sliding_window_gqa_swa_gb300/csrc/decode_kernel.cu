@@ -163,8 +163,13 @@ decode_kernel(const DecodeArgs a) {
   const long long slab = (((long long)a.layer * a.batch + b) * a.kv_heads + h) * (long long)R * D;
   uint16_t* Kc = a.k_cache + slab;
   uint16_t* Vc = a.v_cache + slab;
-  const uint16_t* kn = a.k_new + ((long long)b * a.kv_heads + h) * D;
-  const uint16_t* vn = a.v_new + ((long long)b * a.kv_heads + h) * D;
+  // KV-sharing layer (no k_new / v_new): attend over rows the owning layer's
+  // decode already wrote this step, without appending; the owner may be the
+  // kernel launched just before, so even the cache is read after the wait
+  const bool append = a.k_new != nullptr;
+  if (!append) pdl_wait();
+  const uint16_t* kn = append ? a.k_new + ((long long)b * a.kv_heads + h) * D : nullptr;
+  const uint16_t* vn = append ? a.v_new + ((long long)b * a.kv_heads + h) * D : nullptr;
   const int nspec = min(kStages, nchunks);  // chunks loaded before the mask is known
   // a range that fits in the ring is loaded at once by every thread with
   // 16-byte asynchronous copies (lowest latency); longer ranges stream
@@ -203,7 +208,7 @@ decode_kernel(const DecodeArgs a) {
     // launched just before this one
     pdl_wait();
     // the new row, the mask bytes of the range
-    for (int i = lane; i < D / 8; i += 32) {
+    for (int i = lane; append && i < D / 8; i += 32) {
       reinterpret_cast<uint4*>(kn_s)[i] = reinterpret_cast<const uint4*>(kn)[i];
       reinterpret_cast<uint4*>(vn_s)[i] = reinterpret_cast<const uint4*>(vn)[i];
     }
@@ -256,7 +261,7 @@ decode_kernel(const DecodeArgs a) {
       }
     }
     // append the step's row to the cache (the compute warps read it from kn_s / vn_s)
-    if (state_ok && cur >= r0 && cur < r1) {
+    if (append && state_ok && cur >= r0 && cur < r1) {
       for (int i = lane; i < D / 8; i += 32) {
         reinterpret_cast<uint4*>(Kc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(kn_s)[i];
         reinterpret_cast<uint4*>(Vc + (long long)cur * D)[i] = reinterpret_cast<const uint4*>(vn_s)[i];
@@ -287,7 +292,9 @@ decode_kernel(const DecodeArgs a) {
 #pragma unroll
       for (int e = 0; e < E / 2; ++e) acc[g][e] = 0ull;
     }
-    const int cur_i = cur - r0;  // the step's row within the range (may be outside)
+    // the step's row within the range (may be outside); without an append it
+    // is read from the cache like any other row
+    const int cur_i = append ? cur - r0 : -1;
     int idx = 0;
     for (int c = 0; c < nchunks; ++c) {
       if (!chunk_on[c]) continue;

@@ -242,3 +242,62 @@ def test_graph_replay_matches_eager(swa, ring):
         cache.check()
         results[use_graph] = torch.stack(outs)
     assert np.array_equal(bits(results[False]), bits(results[True]))
+
+
+def test_kv_sharing_layer(swa):
+    """A KV-sharing layer (k_new = v_new = NULL) attends over the owning
+    layer's rows, which already hold the step's token, and appends nothing."""
+    dev = torch.device("cuda")
+    c = synth.decode_case(3400, batch=2, q_heads=4, kv_heads=2, head_dim=256, window=64, prompt_len=150,
+                          steps=90, layers=1)
+    S, W, D, B, Hq, Hkv = c.prompt_len, c.window, c.head_dim, c.batch, c.q_heads, c.kv_heads
+    scale = D ** -0.5
+    gen = torch.Generator().manual_seed(3401)
+    q_share = torch.randn(c.steps, B, Hq, D, generator=gen).to(torch.bfloat16)
+    pre = swa.Cache(swa.CACHE_PREFILL, 1, B, Hkv, D, W, S)
+    swa.prefill(pre, 0, swa.MODE_CAUSAL, torch.zeros(B, S, Hq, D, dtype=torch.bfloat16, device=dev),
+                c.prompt_k[0].to(dev), c.prompt_v[0].to(dev), swa.Meta(B, S, 0, S, W), scale,
+                torch.empty(B, S, Hq, D, dtype=torch.bfloat16, device=dev))
+    cache = swa.Cache(swa.CACHE_COMPACT, 1, B, Hkv, D, W, S)
+    swa.compact(pre, cache)
+    mask = torch.empty(B, cache.rows, dtype=torch.uint8, device=dev)
+    ws = swa.decode_workspace(cache, Hq)
+    model = CompactModel(S, W)
+    own, shared = [], []
+    for t in range(c.steps):
+        if cache.needs_roll():
+            swa.roll(cache)
+            model.roll()
+        swa.build_decode_mask(cache, mask)
+        model.begin_step(np.zeros(B))
+        o1 = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+        o2 = torch.empty_like(o1)
+        swa.decode(cache, 0, c.dec_q[t, 0].to(dev), c.dec_k[t, 0].to(dev), c.dec_v[t, 0].to(dev), mask, scale,
+                   o1, ws)
+        swa.decode(cache, 0, q_share[t].to(dev), None, None, mask, scale, o2, ws)
+        own.append(o1)
+        shared.append(o2)
+    torch.cuda.synchronize()
+    cache.check()
+    # the sharing calls appended nothing: the cache holds exactly the owner's rows
+    for b in range(B):
+        fk, fv = _full_kv(c, b, c.steps)
+        ek = torch.from_numpy(model.expected_cache(fk)).to(torch.bfloat16)
+        assert np.array_equal(bits(cache.k[0, b].transpose(0, 1)), bits(ek))
+    args = (c.prompt_k[0], c.prompt_v[0], None, c.dec_k[:, 0], c.dec_v[:, 0], S, W, scale, c.valid_start.numpy())
+    ro, _ = reference.decode_full(args[0], args[1], c.dec_q[:, 0], *args[3:])
+    rs, _ = reference.decode_full(args[0], args[1], q_share, *args[3:])
+    assert_close(torch.stack(own), ro, "owner")
+    assert_close(torch.stack(shared), rs, "KV-sharing layer")
+
+
+def test_global_layer_as_unbounded_window(swa):
+    """A global (full causal) layer through the same path: a window at least as
+    long as every position the job reaches (W >= S + steps); the rolls then
+    drop only rows of negative positions."""
+    S, T = 150, 130
+    c = synth.decode_case(3500, batch=1, q_heads=4, kv_heads=2, head_dim=256, window=S + T, prompt_len=S,
+                          steps=T, layers=1)
+    _, _, dec_o, dec_l, ref_o, ref_l = run_decode_case(swa, c, check_every_step=False)
+    assert_close(dec_o, ref_o, "global-layer decode")
+    assert_lse(dec_l, ref_l, "global-layer decode lse")
