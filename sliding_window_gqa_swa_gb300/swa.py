@@ -127,13 +127,20 @@ class Cache:
 
     def __init__(self, kind: int, layers: int, batch: int, kv_heads: int, head_dim: int, window: int,
                  prompt_len: int, valid_start: Optional[torch.Tensor] = None, rows: int = 0,
-                 device=None, stream=None):
+                 device=None, stream=None, mem: Optional[torch.Tensor] = None):
+        """``mem``: optional caller-owned uint8 device buffer (>= the cache's bytes,
+        256-byte aligned) to bind instead of a fresh allocation."""
         desc = CacheDesc(kind, layers, batch, kv_heads, head_dim, window, prompt_len, rows)
         nbytes = int(_lib.swa_cache_bytes(ctypes.byref(desc)))
         if nbytes == 0:
             raise SwaError(EINVAL, f"swa_cache_bytes: {last_error()}")
         device = torch.device("cuda") if device is None else torch.device(device)
-        self.mem = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        if mem is not None:
+            if mem.dtype != torch.uint8 or not mem.is_cuda or mem.numel() < nbytes:
+                raise SwaError(EINVAL, f"mem must be a CUDA uint8 tensor of at least {nbytes} bytes")
+            self.mem = mem[:nbytes]
+        else:
+            self.mem = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.valid_start = None
         if valid_start is not None:
             self.valid_start = valid_start.to(device=device, dtype=torch.int32).contiguous()
@@ -228,10 +235,12 @@ def build_decode_mask(cache: Cache, mask_out: torch.Tensor, stream=None) -> None
           "swa_build_mask(decode)")
 
 
-def build_prefill_plan(meta: Meta, cache: Optional[Cache] = None, stream=None, device=None) -> torch.Tensor:
-    """Allocate and build the prefill plan; attaches it to ``meta``."""
+def build_prefill_plan(meta: Meta, cache: Optional[Cache] = None, stream=None, device=None,
+                       out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Build the prefill plan (into ``out`` when given, else a new buffer);
+    attaches it to ``meta``."""
     dev = torch.device("cuda") if device is None else torch.device(device)
-    plan = torch.empty(meta.plan_bytes(), dtype=torch.uint8, device=dev)
+    plan = torch.empty(meta.plan_bytes(), dtype=torch.uint8, device=dev) if out is None else out
     check(_lib.swa_build_mask(cache.handle if cache else None, MASK_PREFILL, ctypes.byref(meta.c),
                               ptr(plan), stream_handle(stream)), "swa_build_mask(prefill)")
     meta.with_plan(plan)
