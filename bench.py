@@ -55,6 +55,17 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of a list of floats over all ranks (identity when
+    torch.distributed is not initialised or has one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -279,16 +290,12 @@ def run_ours(args):
             job.run(evs[k])
         t1.record()
         barrier()
-    total_ms = t0.elapsed_time(t1)
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-
     decode_ms = sum(e["decode_start"].elapsed_time(e["end"]) for e in evs)
     prefill_ms = sum(e["inputs"].elapsed_time(e["prefill"]) for e in evs)
     graph_ms = sum(sum(e["step_s"][t].elapsed_time(e["step_e"][t]) for t in range(T)) for e in evs)
+    # the slowest replica sets every reported time
+    total_ms, decode_ms, prefill_ms, graph_ms = max_over_ranks(
+        [t0.elapsed_time(t1), decode_ms, prefill_ms, graph_ms], dev)
     us_per_layer = decode_ms * 1e3 / (args.steps * T * L)
     launch_us = graph_ms * 1e3 / (args.steps * T * L)  # the shared mask's share is included
     # algorithmic bytes of one decode launch: the W admitted K and V rows of both kv heads,
