@@ -1,38 +1,44 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05): head size
-// 256 in one CTA, head size 512 in a pair of CTAs.
+// Prefill attention on the 5th-generation tensor cores (tcgen05).
 //
 // One CTA computes 128 query rows of one query head, over a 256-column slice
 // of the head dimension, against the key tiles (64 keys each) its rows need;
 // the tile range comes from the causal arithmetic or from the plan built on
-// the device (generic plan: image blocks, documents).
-//
-// Tensor memory (512 columns): O (256 columns, fp32), two S buffers (64
-// columns each) and the CTA's Q slice (128 columns, bf16 pairs), so the
-// score MMAs read only K from shared memory.  Warp roles:
-//   warp 0     TMA producer: K_j and V_j slices into a ring of 32 KB slots
-//              (128-byte swizzled, 64-column boxes), in the order the MMA
-//              warp consumes them: K_0, K_1, then V_j, K_{j+2} for each j;
-//   warp 1     MMA issuer (one thread): S_0 and S_1, then for each tile j one
-//              group that interleaves O += P_j V_j (4 MMAs of 128x256x16, V
-//              read MN-major, P from shared memory) with S_{j+2} = Q K_{j+2}^T
-//              (16 MMAs of 128x64x16, Q from tensor memory) into the S buffer
-//              P_j's scores came from.  The tensor pipe runs consecutive MMAs
-//              of one accumulator back to back only when the MMA is wide;
-//              interleaving the two independent chains keeps it busy;
+// the device (generic plan: image blocks, documents).  Three shapes:
+//   * head size 256, even GQA group (kSm2): the two CTAs of a cluster are
+//     query heads 2g and 2g + 1 of one KV head and share every MMA
+//     (cta_group::2, M = 256).  Each CTA loads half of every K tile (32 keys)
+//     and half of every V tile (128 head-dimension columns).  Tensor memory
+//     per CTA: O (256 columns), three S buffers (64 each), two P buffers (32
+//     each, bf16 pairs; P is the A operand of PV from tensor memory); Q stays
+//     in shared memory;
+//   * head size 256, odd group: one CTA per head (cta_group::1); tensor
+//     memory holds O, two S buffers and the Q slice (128 columns, the A
+//     operand of QK^T); P goes through shared memory;
+//   * head size 512 (kPair): the two CTAs of a cluster hold the two 256-column
+//     halves of the head; each computes a partial S over its half of the
+//     contraction and sends it into one of the peer's two exchange buffers
+//     with asynchronous remote stores; both add the two partials (fp32
+//     addition commutes: the same S bit for bit), run the identical softmax,
+//     and accumulate their own half of O -- no MMA is done twice.
+// Warp roles:
+//   warp 0     TMA producer: K and V slices into a ring of slots (128-byte
+//              swizzled, 64-column boxes), in the order the MMA thread
+//              consumes them: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for each j;
+//   warp 1     one thread issues the MMAs: S_0 .. S_{NS-1}, then for each
+//              tile j one group that interleaves O += P_j V_j (4 MMAs, V read
+//              MN-major) with S_{j+NS} = Q K_{j+NS}^T (16 MMAs of N = 64) into
+//              the S buffer S_j came from.  The tensor pipe runs consecutive
+//              MMAs of one accumulator back to back only when the MMA is
+//              wide; interleaving the two independent chains keeps it busy.
+//              (kSm2: the odd CTA's warp 1 forwards "P_j written" to the
+//              issuing CTA; kPair: warp 10 forwards "exchange buffer read");
 //   warps 2-9  softmax: two warpgroups, one query row per thread (its TMEM
 //              lane); group g owns score columns [32g, 32g + 32) of each tile
-//              and output columns [128g, 128g + 128).  Each thread first
-//              copies its share of the Q row into tensor memory.  Per tile:
-//              apply the row's key interval [lo, hi], take the row maximum,
-//              online softmax in the exp2 domain with lazy rescaling of O
-//              (only when the maximum grows by more than 2^8), write P (bf16)
-//              to shared memory; finally normalise O and store it.
-// Head size 512: the two CTAs of a cluster hold the two column halves.  Each
-// computes a partial S over its half of the contraction and sends it to its
-// peer through distributed shared memory; both add the two partials
-// (fp32 addition commutes, so both obtain the same S bit for bit), run the
-// identical softmax, and accumulate their own half of O -- no MMA is done
-// twice.
+//              and output columns [128g, 128g + 128).  Per tile: apply the
+//              row's key interval [lo, hi], take the row maximum, online
+//              softmax in the exp2 domain with lazy rescaling of O (only when
+//              the maximum grows by more than 2^8), write P (bf16); finally
+//              normalise O and store it.
 // Every wait is bounded; a timeout sets the device error word, makes all
 // roles stop, lets in-flight copies and MMAs finish, and frees TMEM.
 //

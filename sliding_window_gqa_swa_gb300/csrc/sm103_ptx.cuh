@@ -60,18 +60,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster named in `cta_mask`:
-// the tile lands at offset `dst` of each CTA's shared memory and each CTA's
-// mbarrier at offset `bar` receives the transaction bytes.
-__device__ __forceinline__ void tma_load_4d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1,
-                                               int c2, int c3, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "h"(cta_mask)
-      : "memory");
-}
-
 // 1-D bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -85,12 +73,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-// Order this thread's generic-proxy global writes before its later async-proxy
-// (bulk copy) reads of the same addresses.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ clusters
@@ -123,10 +105,6 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ void st_dsmem_f32x4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 // 16-byte store into another CTA's shared memory whose completion is counted
 // (as transaction bytes) on that CTA's mbarrier `bar` (cluster addresses).
 __device__ __forceinline__ void st_async_u32x4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
