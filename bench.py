@@ -46,7 +46,7 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 SPYRE_RUNTIME_MASK_US = 562.0
 # DRAM bytes (read + write) of one launch of the dominant kernel, decode_kernel<256, 2, 16>, from
 # one ncu capture of the current kernel (cold cache); set to None whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = None
+DECODE_TRAFFIC_BYTES = 2299648
 
 
 # ----------------------------------------------------------------------------- helpers
