@@ -154,6 +154,16 @@ decode_kernel(const DecodeArgs a) {
   __shared__ float s_m[kComputeWarps][G], s_l[kComputeWarps][G];
   __shared__ float s_M[G], s_L[G];
   __shared__ int s_last;
+  // cluster merge by pushes: every CTA sends each CTA of the cluster (M, L) and
+  // that CTA's slice of its accumulator with asynchronous remote stores; each
+  // CTA waits for its slice from all and finishes it (no cluster barrier after
+  // the compute).  Used when the slices are equal and fit these buffers.
+  constexpr int kNf = G * D / 4;  // float4s of one CTA's accumulator
+  constexpr bool kPushable = G <= 2 && kNf <= 256;
+  __shared__ __align__(16) float4 s_recv[kPushable ? 16 + kNf : 1];
+  __shared__ __align__(8) uint64_t s_merge_bar;
+  const bool push = kPushable && a.cluster && a.nsplit > 1 && a.nsplit <= 16 && kNf % a.nsplit == 0;
+  const int slice = push ? kNf / a.nsplit : 0;
   const uint32_t sring = smem_u32(smem);
   const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kStages);
 
@@ -194,6 +204,10 @@ decode_kernel(const DecodeArgs a) {
         mbar_init(bar_empty0 + 8 * s, kComputeWarps);
       }
       *abort_flag = 0;
+      if (push) {  // phase 0 completes when every CTA's slice (header + accumulator) landed
+        mbar_init(smem_u32(&s_merge_bar), 1);
+        mbar_arrive_expect_tx(smem_u32(&s_merge_bar), uint32_t(a.nsplit * (1 + slice) * 16));
+      }
       fence_mbar_init();
       for (int c = 0; c < (oneshot ? 0 : nspec); ++c) {
         const uint32_t bytes = uint32_t(min(CH, nrows - c * CH)) * D * 2;
@@ -231,6 +245,8 @@ decode_kernel(const DecodeArgs a) {
   const bool state_ok = cur >= 0 && cur < R;
   if (oneshot) cp_async_wait_all();
   __syncthreads();
+  // the merge barrier is initialised: peers may push once they pass the matching wait
+  if (push) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (warp == kComputeWarps) {
     for (int c = lane; c < nchunks; c += 32) {
       uint8_t any = 0;
@@ -487,6 +503,57 @@ decode_kernel(const DecodeArgs a) {
       }
       if (tid < G && a.lse)
         a.lse[head0 + tid] = s_L[tid] > 0.f ? (s_M[tid] + log2f(s_L[tid])) * 0.69314718055994530942f : -CUDART_INF_F;
+    }
+    return;
+  }
+
+  if (push) {
+    // ---- cluster merge by pushes (see s_recv)
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    const int rank = int(cluster_ctarank());
+    const float4* acc4 = reinterpret_cast<const float4*>(cta_acc);
+    for (int x = tid; x < nsplit * (1 + slice); x += kThreads) {
+      const int k = x / (1 + slice), j = x % (1 + slice);
+      // item 0 of each destination: this CTA's (M, L) per query head
+      const float4 val = (j == 0) ? make_float4(s_M[0], s_L[0], s_M[G - 1], s_L[G - 1]) : acc4[k * slice + j - 1];
+      st_async_u32x4(map_shared(smem_u32(&s_recv[rank * (1 + slice) + j]), uint32_t(k)), __float_as_uint(val.x),
+                     __float_as_uint(val.y), __float_as_uint(val.z), __float_as_uint(val.w),
+                     map_shared(smem_u32(&s_merge_bar), uint32_t(k)));
+    }
+    // this CTA's slice from every CTA of the cluster (bounded wait)
+    bool got = true;
+    if (tid < slice) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!(got = mbar_try_wait(smem_u32(&s_merge_bar), 0)) && globaltimer_ns() - t0 < 2000000000ull) {
+      }
+      if (!got) atomicCAS(&st->error, 0, kErrTimeout);
+    }
+    if (tid < slice && got && !aborted) {
+      const int f = rank * slice + tid;
+      const int g = (4 * f) / D;
+      float M = -CUDART_INF_F;
+      for (int r = 0; r < nsplit; ++r) {
+        const float4 hdr = s_recv[r * (1 + slice)];
+        M = fmaxf(M, g ? hdr.z : hdr.x);
+      }
+      float L = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < nsplit; ++r) {  // fixed order: CTA rank
+        const float4 hdr = s_recv[r * (1 + slice)];
+        const float ms = g ? hdr.z : hdr.x, ls = g ? hdr.w : hdr.y;
+        const float w = (ms == -CUDART_INF_F) ? 0.f : exp2f(ms - M);
+        const float4 v = s_recv[r * (1 + slice) + 1 + tid];
+        L += w * ls;
+        o.x = fmaf(w, v.x, o.x);
+        o.y = fmaf(w, v.y, o.y);
+        o.z = fmaf(w, v.z, o.z);
+        o.w = fmaf(w, v.w, o.w);
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      reinterpret_cast<uint2*>(a.out + head0 * D)[f] =
+          make_uint2(pack_bf16(o.x * inv, o.y * inv), pack_bf16(o.z * inv, o.w * inv));
+      if (a.lse && 4 * f == g * D)
+        a.lse[head0 + g] = L > 0.f ? (M + log2f(L)) * 0.69314718055994530942f : -CUDART_INF_F;
     }
     return;
   }
