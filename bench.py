@@ -164,8 +164,10 @@ def ev():
 class SingleStreamJob:
     """The whole single-stream job on one GPU (one bench step)."""
 
-    def __init__(self, swa, case, dev, e2e=False, ring=False):
+    def __init__(self, swa, case, dev, e2e=False, ring=False, l2_flush=None):
         self.swa, self.dev, self.e2e = swa, dev, e2e
+        # optional scratch buffer larger than L2, overwritten before every decode step's graph
+        self.l2_flush = l2_flush
         c = case
         self.L, self.S, self.W, self.D = c.layers, c.prompt_len, c.window, c.head_dim
         self.B, self.Hq, self.Hkv, self.T = c.batch, c.q_heads, c.kv_heads, c.steps
@@ -242,6 +244,8 @@ class SingleStreamJob:
             self.qb.copy_(self.dq[t], non_blocking=True)
             self.kb.copy_(self.dk[t], non_blocking=True)
             self.vb.copy_(self.dv[t], non_blocking=True)
+            if self.l2_flush is not None:
+                self.l2_flush.fill_(t & 127)
             e["step_s"][t].record()
             if self.graph is None:
                 self.graph = self._capture()
@@ -306,6 +310,8 @@ def run_ours(args):
     pre_flops = 4.0 * job.D * job.Hq * causal_pairs(job.S, job.W) * job.B * L
     pre_tflops = pre_flops / (prefill_ms / args.steps * 1e-3) / 1e12
     launches = job.launches * args.steps
+    warm_step_med = statistics.median(
+        e["step_s"][t].elapsed_time(e["step_e"][t]) for e in evs for t in range(T))
     del job
     torch.cuda.empty_cache()
 
@@ -348,6 +354,29 @@ def run_ours(args):
             "decode_launch_us": round(r_graph * 1e3 / (args.steps * T * L), 4),
             "anchored_us_per_layer": round(us_per_layer, 4)}
         del rjob
+        torch.cuda.empty_cache()
+        # the same job with L2 flushed before every step: a 2 x L2 scratch write evicts the
+        # compact cache, q/k/v and the state, so each step's graph starts from HBM
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        cjob = SingleStreamJob(swa, case, dev, l2_flush=flush)
+        for _ in range(max(1, min(args.warmup, 2))):
+            cjob.run(cjob.make_events())
+        torch.cuda.synchronize()
+        cev = [cjob.make_events() for _ in range(args.steps)]
+        for k in range(args.steps):
+            cjob.run(cev[k])
+        torch.cuda.synchronize()
+        cold_med = statistics.median(
+            e["step_s"][t].elapsed_time(e["step_e"][t]) for e in cev for t in range(T))
+        secondary["single_stream_l2_cold"] = {
+            "workload": "the single-stream job with L2 flushed (a write of 2 x L2 bytes) before every decode step",
+            "us_per_layer": round(cold_med * 1e3 / L, 4),
+            "warm_us_per_layer": round(warm_step_med * 1e3 / L, 4),
+            "timing": "median over all steps of the step graph (shared mask + one decode per layer) / layers; "
+                      "the flush runs before the step's start event",
+            "flush_bytes": int(2 * l2)}
+        del cjob, flush
         torch.cuda.empty_cache()
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

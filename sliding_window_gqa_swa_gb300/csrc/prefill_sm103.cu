@@ -73,18 +73,23 @@ constexpr int KV_CHUNK = BN * 128;  // one 64-column box of K or V: 8 KB
 constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
 constexpr int Q_CHUNK = BM * 128;  // one 64-column box of Q: 16 KB
-constexpr int Q_BYTES = Q_CHUNK * (HS / 64);
 constexpr int XS_BYTES = BM * BN * 4;  // one partial-S exchange buffer (head size 512; two of them)
 
 // kSm2: the CTA pair shares its MMAs (cta_group::2) and each CTA holds half
-// of every K/V tile: 32 keys of K, 128 head-dimension columns of V.  Its Q
-// slice stays in shared memory, which frees tensor memory for a third S buffer;
-// P lives in tensor memory (two 32-column buffers after the S buffers).
-template <bool kPair, bool kSm2>
+// of every K/V tile: 32 keys of K (one slot per 256 contraction columns), 128
+// head-dimension columns of V (one slot).  Its whole Q row tile (the
+// contraction, 256 or 512 columns: kWide) stays in shared memory; tensor
+// memory holds O and two S buffers, each split into the partial sums over the
+// two halves of the contraction, and P overwrites the S columns it came from.
+template <bool kPair, bool kSm2, bool kWide>
 struct Layout {
-  static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;  // one ring slot
-  static constexpr int NST = kPair ? 4 : (kSm2 ? 10 : 6);      // K/V ring stages
-  static constexpr int NS = kSm2 ? 3 : 2;                      // S buffers in TMEM
+  static constexpr int HQK = kWide ? 2 * HS : HS;                // contraction columns per CTA
+  static constexpr int Q_BYTES = Q_CHUNK * (HQK / 64);
+  static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;    // one ring slot
+  static constexpr int KSLOTS = kWide ? 2 : 1;                   // ring slots of one K tile
+  static constexpr int NST = kPair ? 4 : (kSm2 ? (kWide ? 6 : 10) : 6);  // ring slots
+  static constexpr int NS = 2;                                   // S buffers in TMEM
+  static constexpr int SB = kSm2 ? 2 * BN : BN;                  // TMEM columns of one S buffer
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + (kSm2 ? Q_BYTES : 0);
   static constexpr int OFF_P = OFF_KV + NST * SLOT;
@@ -97,16 +102,16 @@ struct Layout {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// TMEM columns: O, then the S buffers (TM_S + b * BN), then the Q slice when
+// TMEM columns: O, then the S buffers (TM_S + b * SB), then the Q slice when
 // it lives in tensor memory (single CTA: after two S buffers)
-constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_P = HS + 3 * BN, TM_COLS = 512;
+constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
 constexpr uint32_t IDESC_QK2 = idesc_bf16_f32(2 * BM, BN, false);  // CTA pair: 256 query rows
 constexpr uint32_t IDESC_PV2 = idesc_bf16_f32(2 * BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-static_assert(TM_Q + HS / 2 <= TM_COLS && TM_P + BN <= TM_COLS, "TMEM budget");
+static_assert(TM_Q + HS / 2 <= TM_COLS && TM_S + 2 * (2 * BN) <= TM_COLS, "TMEM budget");
 
 template <int NST>
 struct Bars {
@@ -114,7 +119,7 @@ struct Bars {
   __device__ uint32_t full(int s) const { return base + 8 * s; }
   __device__ uint32_t empty(int s) const { return base + 8 * (NST + s); }
   __device__ uint32_t q() const { return base + 8 * (2 * NST); }  // Q slice ready for the MMAs
-  __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }  // b < 3
+  __device__ uint32_t s_full(int b) const { return base + 8 * (2 * NST + 1 + b); }  // b < 2
   __device__ uint32_t p_full(int b) const { return base + 8 * (2 * NST + 4 + b); }
   __device__ uint32_t pv_done(int b) const { return base + 8 * (2 * NST + 6 + b); }
   __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 8); }
@@ -177,14 +182,16 @@ __device__ __forceinline__ float mask_max(uint32_t* sr, int kbase, int lo, int h
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
-template <bool kPair, bool kSm2>
+template <bool kPair, bool kSm2, bool kWide>
 __global__ void __launch_bounds__(threads_of(kPair), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  using LY = Layout<kPair, kSm2>;
-  static_assert(!(kPair && kSm2), "the pair MMA serves head size 256 only");
+  using LY = Layout<kPair, kSm2, kWide>;
+  static_assert(!(kPair && kSm2) && (kSm2 || !kWide), "shape");
   constexpr int NST = LY::NST;
   constexpr int NS = LY::NS;
+  constexpr int SB = LY::SB;
+  constexpr int KSLOTS = LY::KSLOTS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -196,14 +203,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   int32_t* err = a.err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int half = kPair ? int(cluster_ctarank()) : 0;  // which column half of the head
-  const int peer = half ^ 1;
-  const int col0 = half * HS;
-  const int hq = kPair ? int(blockIdx.x >> 1) : int(blockIdx.x);
   // kSm2: the cluster's two CTAs are query heads 2g and 2g + 1 of one KV head
-  // (same rows, same key tiles); the even CTA issues the pair MMAs
+  // (same rows, same key tiles); the even CTA issues the pair MMAs.  kWide:
+  // consecutive clusters take the two 256-column halves of O (both compute the
+  // same S over the whole contraction)
   const int crank = kSm2 ? int(cluster_ctarank()) : 0;
   const bool issuer = crank == 0;
+  const int half = kPair ? int(cluster_ctarank()) : (kWide ? int(blockIdx.x >> 1) & 1 : 0);  // column half of O
+  const int peer = half ^ 1;
+  const int col0 = half * HS;
+  const int hq = kPair ? int(blockIdx.x >> 1)
+                       : (kWide ? 2 * int(blockIdx.x >> 2) + crank : int(blockIdx.x));
   const int qt = blockIdx.y, b = blockIdx.z;
   const int hk = hq / (a.q_heads / a.kv_heads);
   const int i0 = qt * BM;
@@ -239,7 +249,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // single CTA: the softmax threads copy Q into TMEM; kSm2: both CTAs' Q
     // tiles complete on the issuing CTA's barrier
     mbar_init(bars.q(), kSm2 ? 1 : 256);
-    for (int i = 0; i < 3; ++i) mbar_init(bars.s_full(i), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(bars.s_full(i), 1);
     for (int i = 0; i < 2; ++i) {
       // kSm2: the issuing CTA also counts the one arrival its peer forwards
       mbar_init(bars.p_full(i), kSm2 && issuer ? 257 : 256);
@@ -279,16 +289,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // ring order: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for j = 0 .. n-1
+    // ring order: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for j = 0 .. n-1 (a K
+    // tile takes KSLOTS consecutive slots)
     if (n > 0) {
       bool ok = true;
       int idx = 0;
       if (kSm2 && lane == 0) {  // this CTA's Q rows; both tiles complete on the issuer's barrier
-        if (issuer) mbar_arrive_expect_tx(bars.q(), 2 * Q_BYTES);
-        for (int c = 0; c < HS / 64; ++c)
-          tma_load_4d_pair(sQ + c * Q_CHUNK, &tm_q, map_shared(bars.q(), 0), col0 + 64 * c, i0, hq, b);
+        if (issuer) mbar_arrive_expect_tx(bars.q(), 2 * LY::Q_BYTES);
+        for (int c = 0; c < LY::HQK / 64; ++c)
+          tma_load_4d_pair(sQ + c * Q_CHUNK, &tm_q, map_shared(bars.q(), 0), 64 * c, i0, hq, b);
       }
-      auto load = [&](int tile, bool is_v) {
+      // part < 0: V_tile; part >= 0: contraction columns [256 part, 256 part + 256) of K_tile
+      auto load = [&](int tile, int part) {
+        const bool is_v = part < 0;
         const int s = idx % NST;
         ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
         if (ok && lane == 0) {
@@ -299,11 +312,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint32_t bar = map_shared(bars.full(s), 0);
             if (issuer) mbar_arrive_expect_tx(bars.full(s), 2 * LY::SLOT);
             if (is_v) {
-              for (int c = 0; c < 2; ++c)  // head-dimension columns [128 crank, 128 crank + 128)
-                tma_load_4d_pair(dst + c * KV_CHUNK, &tm_v, bar, 128 * crank + 64 * c, k0, hk, b);
+              for (int c = 0; c < 2; ++c)  // head-dimension columns col0 + [128 crank, 128 crank + 128)
+                tma_load_4d_pair(dst + c * KV_CHUNK, &tm_v, bar, col0 + 128 * crank + 64 * c, k0, hk, b);
             } else {
               for (int c = 0; c < HS / 64; ++c)  // keys [k0 + 32 crank, k0 + 32 crank + 32)
-                tma_load_4d_pair(dst + c * (KV_CHUNK / 2), &tm_k, bar, 64 * c, k0 + (BN / 2) * crank, hk, b);
+                tma_load_4d_pair(dst + c * (KV_CHUNK / 2), &tm_k, bar, HS * part + 64 * c, k0 + (BN / 2) * crank,
+                                 hk, b);
             }
           } else {
             mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
@@ -315,10 +329,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
         ++idx;
       };
-      for (int t = 0; t < NS && t < n && ok; ++t) load(t, false);
+      for (int t = 0; t < NS && t < n && ok; ++t)
+        for (int part = 0; part < KSLOTS && ok; ++part) load(t, part);
       for (int j = 0; j < n && ok; ++j) {
-        load(j, true);
-        if (j + NS < n && ok) load(j + NS, false);
+        load(j, -1);
+        if (j + NS < n)
+          for (int part = 0; part < KSLOTS && ok; ++part) load(j + NS, part);
       }
     }
   } else if (warp == 1) {
@@ -326,25 +342,99 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // one thread issues every MMA; the other lanes of the warp stay idle
     if (n > 0 && issuer && lane == 0) {
       bool ok = wait_bar<kSm2>(bars.q(), 0, abort_flag, err);
-      // kK: bytes between the 64-column boxes of a K slot
-      constexpr int kK = kSm2 ? KV_CHUNK / 2 : KV_CHUNK;
-      // one K=16 step of S_b = Q K^T into S buffer b; K (K-major) from ring slot
-      // kslot; Q from TMEM (single CTA) or from shared memory (kSm2)
-      auto qk_step = [&](int sbuf, uint32_t kslot, int kk) {
-        const int c = kk >> 2, sub = kk & 3;
-        const uint64_t bd = sdesc_sw128(kslot + c * kK + sub * 32, 16, 1024);
-        const uint32_t d = tmem + TM_S + sbuf * BN;
-        if (kSm2)
-          mma_pair_bf16_ss(d, sdesc_sw128(sQ + c * Q_CHUNK + sub * 32, 16, 1024), bd, IDESC_QK2, kk > 0 ? 1u : 0u);
-        else
-          mma_bf16_ts(d, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
-      };
       // completion of the MMAs issued so far, on `bar` of both CTAs (kSm2) or of this CTA
       auto commit = [&](uint32_t bar) {
         if (kSm2)
           mma_pair_commit(bar, 0x3);
         else
           mma_commit(bar);
+      };
+      if constexpr (kSm2) {
+        // S_t is the sum of two independent chains of NH K=16 steps, one per
+        // half of the contraction, into the lo and hi partials of S buffer
+        // t & 1; issuing them alternately keeps two accumulations in flight.
+        constexpr int NH = LY::HQK / 32;
+        // contraction step kk: Q box kk / 4 (shared memory); K from slot part
+        // kk / 16 of the tile (32 keys, four 64-column boxes of 4 KB)
+        auto qk2 = [&](int sbuf, const uint32_t* ks, int kk) {
+          const int part = kWide ? (kk >> 4) : 0, kl = kk & 15;
+          const uint64_t bd = sdesc_sw128(ks[part] + (kl >> 2) * (KV_CHUNK / 2) + (kl & 3) * 32, 16, 1024);
+          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * Q_CHUNK + (kk & 3) * 32, 16, 1024);
+          mma_pair_bf16_ss(tmem + TM_S + sbuf * SB + (kk >= NH ? BN : 0), ad, bd, IDESC_QK2, (kk % NH) ? 1u : 0u);
+        };
+        int idx = 0;
+        for (int t = 0; t < NS && t < n && ok; ++t) {
+          uint32_t ks[2] = {0u, 0u};
+          for (int part = 0; part < KSLOTS && ok; ++part) {
+            const int s = (idx + part) % NST;
+            ok = wait_bar(bars.full(s), ((idx + part) / NST) & 1, abort_flag, err);
+            ks[part] = sKV + s * LY::SLOT;
+          }
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < NH; ++k) {
+            qk2(t, ks, k);
+            qk2(t, ks, NH + k);
+          }
+          commit(bars.s_full(t));
+          for (int part = 0; part < KSLOTS; ++part) commit(bars.empty((idx + part) % NST));
+          idx += KSLOTS;
+        }
+        for (int j = 0; j < n && ok; ++j) {
+          const int sb = j & 1;
+          const bool next = j + NS < n;  // S_{j+2} goes to the buffer S_j came from
+          const int sv = idx % NST;
+          // P_j written (so S_j read), V_j and K_{j+2} loaded: one round of polls,
+          // then bounded waits for whatever is still pending
+          bool rdy = mbar_try_wait_cluster(bars.p_full(sb), (j >> 1) & 1) &&
+                     mbar_try_wait(bars.full(sv), (idx / NST) & 1);
+          for (int part = 0; next && rdy && part < KSLOTS; ++part)
+            rdy = mbar_try_wait(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1);
+          if (!rdy) {
+            ok = wait_bar<true>(bars.p_full(sb), (j >> 1) & 1, abort_flag, err) &&
+                 wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err);
+            for (int part = 0; next && ok && part < KSLOTS; ++part)
+              ok = wait_bar(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1, abort_flag, err);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const uint32_t ks[2] = {sKV + ((idx + 1) % NST) * LY::SLOT, sKV + ((idx + 2) % NST) * LY::SLOT};
+          const uint32_t vslot = sKV + sv * LY::SLOT;
+          const uint32_t sbase = tmem + TM_S + sb * SB;
+#pragma unroll
+          for (int p = 0; p < BN / 16; ++p) {
+            // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
+            // 8-key row groups 1024 B apart.  P_j from TMEM: softmax group p / 2
+            // left its 32 keys in the first 16 columns of its 32-column slice of
+            // the lo partial; 8 columns (16 keys) per step
+            const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
+            mma_pair_bf16_ts(tmem + TM_O, sbase + 32 * (p >> 1) + 8 * (p & 1), bd, IDESC_PV2,
+                             (j > 0 || p > 0) ? 1u : 0u);
+            if (next) qk2(sb, ks, NH + p);  // the hi chain does not touch P_j
+          }
+          if (next) {
+            // the lo chain overwrites P_j: issued after the last PV step (the
+            // tensor pipe executes one thread's MMAs in order)
+#pragma unroll
+            for (int k = 0; k < NH; ++k) {
+              qk2(sb, ks, k);
+              if (4 + k < NH) qk2(sb, ks, NH + 4 + k);
+            }
+            commit(bars.s_full(sb));
+          }
+          commit(bars.pv_done(sb));
+          commit(bars.empty(sv));
+          for (int part = 0; next && part < KSLOTS; ++part) commit(bars.empty((idx + 1 + part) % NST));
+          idx += 1 + (next ? KSLOTS : 0);
+        }
+      } else {
+      // one K=16 step of S_b = Q K^T into S buffer b; K (K-major) from ring slot
+      // kslot; Q from TMEM
+      auto qk_step = [&](int sbuf, uint32_t kslot, int kk) {
+        const int c = kk >> 2, sub = kk & 3;
+        const uint64_t bd = sdesc_sw128(kslot + c * KV_CHUNK + sub * 32, 16, 1024);
+        mma_bf16_ts(tmem + TM_S + sbuf * BN, tmem + TM_Q + kk * 8, bd, IDESC_QK, kk > 0 ? 1u : 0u);
       };
       int idx = 0;
       for (int t = 0; t < NS && t < n && ok; ++t) {
@@ -365,12 +455,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int sv = idx % NST, sk = (idx + 1) % NST;
         // P_j written (so S_j read), V_j and K_{j+NS} loaded: one round of polls,
         // then bounded waits for whatever is still pending
-        const bool pf = kSm2 ? mbar_try_wait_cluster(bars.p_full(pb), (j >> 1) & 1)
-                             : mbar_try_wait(bars.p_full(pb), (j >> 1) & 1);
+        const bool pf = mbar_try_wait(bars.p_full(pb), (j >> 1) & 1);
         const bool vf = mbar_try_wait(bars.full(sv), (idx / NST) & 1);
         const bool kf = !next || mbar_try_wait(bars.full(sk), ((idx + 1) / NST) & 1);
         if (!(pf & vf & kf)) {
-          ok = wait_bar<kSm2>(bars.p_full(pb), (j >> 1) & 1, abort_flag, err) &&
+          ok = wait_bar(bars.p_full(pb), (j >> 1) & 1, abort_flag, err) &&
                wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err) &&
                (!next || wait_bar(bars.full(sk), ((idx + 1) / NST) & 1, abort_flag, err));
           if (!ok) break;
@@ -382,12 +471,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
           // 8-key row groups 1024 B apart
           const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
-          if (kSm2)  // P_j from TMEM: 8 columns (16 keys) per step
-            mma_pair_bf16_ts(tmem + TM_O, tmem + TM_P + pb * (BN / 2) + p * 8, bd, IDESC_PV2,
-                             (j > 0 || p > 0) ? 1u : 0u);
-          else
-            mma_bf16_ss(tmem + TM_O, sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024), bd, IDESC_PV,
-                        (j > 0 || p > 0) ? 1u : 0u);
+          mma_bf16_ss(tmem + TM_O, sdesc_sw128(sP + pb * P_BYTES + p * 32, 16, 1024), bd, IDESC_PV,
+                      (j > 0 || p > 0) ? 1u : 0u);
           if (next) {
 #pragma unroll
             for (int kk = 4 * p; kk < 4 * p + 4; ++kk) qk_step(sbuf, kslot, kk);
@@ -398,6 +483,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         commit(bars.empty(sv));
         if (next) commit(bars.empty(sk));
         idx += next ? 2 : 1;
+      }
       }
     } else if (kSm2 && n > 0 && !issuer) {
       // the peer CTA forwards each P_j's readiness to the issuing CTA with one
@@ -481,54 +567,73 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // the tensor core accumulates from the same rounded values); l_exact sums
     // the unrounded ones (gives the lse)
     float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
+    // The two warps of a row (one per group) meet at a named barrier for every
+    // tile in the pair kernels; a warp that gives up (timeout or abort) keeps
+    // meeting its partner there and skips the rest of each tile, so the
+    // barrier's arrivals stay paired and every role reaches the teardown.
+    constexpr bool kExchange = kPair || kSm2;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const int sb = t % NS, pb = t & 1;
-      ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tmem + lane_off + TM_S + sb * BN;
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
+      if (!kExchange && !ok) break;
+      if (ok) tc_fence_after();
+      const uint32_t tS = tmem + lane_off + TM_S + sb * SB;
       const int k0 = (kt_lo + t) * BN;
       // the masking pass runs only when some row of the warp needs it
       const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
       // sr[0, HC): this group's columns; single CTA: sr[HC, BN) the other group's
-      uint32_t sr[kPair ? HC : BN];
+      uint32_t sr[kExchange ? HC : BN];
       float mraw = -CUDART_INF_F;
-      if constexpr (kPair) {
-        tmem_ld32(tS + cb, sr);
-        tmem_ld_wait();
-        // send my partial slice into the peer's exchange buffer xb (once the peer
-        // has consumed what this CTA sent there two tiles ago); the stores count
-        // their bytes on the peer's xs_full(xb)
-        const int xb = t & 1;
-        if (t >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(xb), ((t >> 1) - 1) & 1, abort_flag, err));
-          if (!ok) break;
-        }
-        const uint32_t fbar = map_shared(bars.xs_full(xb), peer);
+      if constexpr (kExchange) {
+        if (ok) {
+          tmem_ld32(tS + cb, sr);
+          if constexpr (kSm2) {
+            // S = lo + hi partial sums (fp32, the same order in both CTAs of a
+            // column-half pair, so they see the same S bit for bit)
+            uint32_t hr[HC];
+            tmem_ld32(tS + BN + cb, hr);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < HC; c += 4)
-          st_async_u32x4(xs_row_peer + xb * XS_BYTES + c * 4, sr[c], sr[c + 1], sr[c + 2], sr[c + 3], fbar);
-        // this CTA receives one whole partial tile per tile
-        if (threadIdx.x == 64) mbar_arrive_expect_tx(bars.xs_full(xb), XS_BYTES);
-        ok = __all_sync(0xffffffffu, wait_bar(bars.xs_full(xb), (t >> 1) & 1, abort_flag, err));
-        if (!ok) break;
-        const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS + xb * XS_BYTES) + r * BN + cb;
+            for (int c = 0; c < HC; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) + __uint_as_float(hr[c]));
+          } else {
+            tmem_ld_wait();
+            // send my partial slice into the peer's exchange buffer xb (once the
+            // peer has consumed what this CTA sent there two tiles ago); the
+            // stores count their bytes on the peer's xs_full(xb)
+            const int xb = t & 1;
+            if (t >= 2)
+              ok = __all_sync(0xffffffffu, wait_bar<true>(bars.xs_free(xb), ((t >> 1) - 1) & 1, abort_flag, err));
+            if (ok) {
+              const uint32_t fbar = map_shared(bars.xs_full(xb), peer);
 #pragma unroll
-        for (int c = 0; c < HC; c += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(xr + c);
-          sr[c] = __float_as_uint(__uint_as_float(sr[c]) + v.x);
-          sr[c + 1] = __float_as_uint(__uint_as_float(sr[c + 1]) + v.y);
-          sr[c + 2] = __float_as_uint(__uint_as_float(sr[c + 2]) + v.z);
-          sr[c + 3] = __float_as_uint(__uint_as_float(sr[c + 3]) + v.w);
+              for (int c = 0; c < HC; c += 4)
+                st_async_u32x4(xs_row_peer + xb * XS_BYTES + c * 4, sr[c], sr[c + 1], sr[c + 2], sr[c + 3], fbar);
+              // this CTA receives one whole partial tile per tile
+              if (threadIdx.x == 64) mbar_arrive_expect_tx(bars.xs_full(xb), XS_BYTES);
+              ok = __all_sync(0xffffffffu, wait_bar(bars.xs_full(xb), (t >> 1) & 1, abort_flag, err));
+            }
+            if (ok) {
+              const float* xr = reinterpret_cast<const float*>(gbase + LY::OFF_XS + xb * XS_BYTES) + r * BN + cb;
+#pragma unroll
+              for (int c = 0; c < HC; c += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(xr + c);
+                sr[c] = __float_as_uint(__uint_as_float(sr[c]) + v.x);
+                sr[c + 1] = __float_as_uint(__uint_as_float(sr[c + 1]) + v.y);
+                sr[c + 2] = __float_as_uint(__uint_as_float(sr[c + 2]) + v.z);
+                sr[c + 3] = __float_as_uint(__uint_as_float(sr[c + 3]) + v.w);
+              }
+              mbar_arrive(bars.xs_cons(xb));  // the forwarding warp tells the peer
+            }
+          }
+          if (ok) mraw = mask_max<HC>(sr, k0 + cb, lo, hi, masked);
         }
-        mbar_arrive(bars.xs_cons(xb));  // the forwarding warp tells the peer
-        mraw = mask_max<HC>(sr, k0 + cb, lo, hi, masked);
         // the two groups of this row agree on the tile maximum
         pmax[grp * BM + r] = mraw;
         named_sync(bar_id);
         mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
         named_sync(bar_id);
+        if (!ok) continue;
       } else {
         // both groups read the whole S row and take its maximum themselves
         tmem_ld32(tS + cb, sr);
@@ -542,7 +647,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
       if (__any_sync(0xffffffffu, rescale)) {
         ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
-        if (!ok) break;
+        if (!ok) {
+          if constexpr (kExchange) continue;
+          else break;
+        }
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
         for (int c0 = grp * OC; c0 < grp * OC + OC; c0 += 32) {
@@ -576,15 +684,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       l_run += ls[0] + ls[1];
       l_exact += es[0] + es[1];
-      if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
-        ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
-        if (!ok) break;
-      }
       if constexpr (kSm2) {
-        // this group's 32 keys = 16 bf16 pairs of the row's P buffer in TMEM
-        tmem_st16(tmem + lane_off + TM_P + pb * (BN / 2) + grp * (HC / 2), pk);
+        // P_t over the first 16 columns of this group's slice of the lo partial
+        // (already read); PV_{t-2}, the last reader of those columns, completed
+        // before S_t did
+        tmem_st16(tS + cb, pk);
         tmem_st_wait();
       } else {
+        if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
+          ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
+          if (!ok) {
+            if constexpr (kExchange) continue;
+            else break;
+          }
+        }
         uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -690,21 +803,23 @@ bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const ui
   return r == CUDA_SUCCESS;
 }
 
-template <bool kPair, bool kSm2>
+template <bool kPair, bool kSm2, bool kWide>
 cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
                         cudaStream_t s) {
+  using LY = Layout<kPair, kSm2, kWide>;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair, kSm2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    Layout<kPair, kSm2>::SMEM);
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair, kSm2, kWide>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int nqt = (a.chunk_len + BM - 1) / BM;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.q_heads * (kPair ? 2 : 1), nqt, a.batch);
+  // head size 512: two CTAs per query head (the two column halves of O)
+  cfg.gridDim = dim3(a.q_heads * (kPair || kWide ? 2 : 1), nqt, a.batch);
   cfg.blockDim = dim3(threads_of(kPair));
-  cfg.dynamicSmemBytes = Layout<kPair, kSm2>::SMEM;
+  cfg.dynamicSmemBytes = LY::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   if (kPair || kSm2) {
@@ -715,7 +830,7 @@ cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
     cfg.attrs = at;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair, kSm2>, mq, mk, mv, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair, kSm2, kWide>, mq, mk, mv, a);
 }
 
 }  // namespace
@@ -726,7 +841,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   // query heads 2g and 2g + 1 share a KV head when the group size is even:
   // their CTAs then form a pair that shares its MMAs and K/V tiles
-  const bool sm2 = a.head_dim == 256 && (a.q_heads / a.kv_heads) % 2 == 0;
+  const bool sm2 = (a.q_heads / a.kv_heads) % 2 == 0;
   // K / V: dims {D, key rows, Hkv, B} with the caller's strides
   const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
   const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
@@ -737,8 +852,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
   const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
   if (!make_map(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
-  if (a.head_dim == 512) return launch_kind<true, false>(mq, mk, mv, a, s);
-  return sm2 ? launch_kind<false, true>(mq, mk, mv, a, s) : launch_kind<false, false>(mq, mk, mv, a, s);
+  if (a.head_dim == 512)
+    return sm2 ? launch_kind<false, true, true>(mq, mk, mv, a, s) : launch_kind<true, false, false>(mq, mk, mv, a, s);
+  return sm2 ? launch_kind<false, true, false>(mq, mk, mv, a, s) : launch_kind<false, false, false>(mq, mk, mv, a, s);
 }
 
 }  // namespace swa

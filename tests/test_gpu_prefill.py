@@ -79,12 +79,18 @@ CASES = {
     # size is even, and one CTA per head otherwise
     "gqa3_single_cta": (4111, 1, 6, 2, 256, 96, 260, 260, 5, None),
     "gqa4_pairs": (4112, 1, 8, 2, 256, 96, 260, 130, 5, None),
+    # head size 512: an even group runs as head pairs (two clusters per pair of
+    # heads, one per half of the output columns); an odd group as column pairs
+    # that exchange partial scores
+    "d512_gqa3_column_pairs": (4113, 1, 3, 1, 512, 64, 200, 200, 7, None),
+    "d512_gqa4_pairs": (4114, 1, 8, 2, 512, 96, 260, 130, 5, None),
 }
 
 # query scale that spreads scores over a wide range, so the running maximum of
 # a row keeps growing across key tiles (exercises the rescaling of the output)
-Q_SCALE = {"causal_big_scores": 4.0}
+Q_SCALE = {"causal_big_scores": 4.0, "causal_big_scores_d512": 3.0}
 CASES["causal_big_scores"] = (4110, 2, 4, 2, 256, 300, 400, 400, 9, None)
+CASES["causal_big_scores_d512"] = (4115, 1, 4, 2, 512, 300, 400, 400, 9, None)
 
 
 @pytest.mark.parametrize("name", list(CASES))
