@@ -13,6 +13,8 @@ What it computes, and where each rule comes from:
                    full-length cache.
 * ``attention`` -- masked softmax attention in float64 over an explicit key
                    set, with query heads sharing key/value heads (GQA).
+* ``backward``  -- the gradients of that attention with respect to q, k and v
+                   (the derivative of the forward definition, written out).
 * ``compact``   -- an integer model of the anchored W+64-row compact cache:
                    the compaction at first decode, the row written by each
                    decode step, the runtime decode mask, and the roll every 64
@@ -36,4 +38,4 @@ code to the stated reading, not the reading to the pages): the window width
 (origin = S - W), and the softmax scale (an argument, default 1/sqrt(D)).
 """
 
-from . import masks, attention, compact, reference  # noqa: F401
+from . import masks, attention, backward, compact, reference  # noqa: F401

@@ -10,6 +10,9 @@ compact-cache index model (``compact``):
                               straddle a chunk).
 * :func:`prefill_rows`     -- the same for selected query rows only.
 * :func:`varlen_rows`      -- packed documents given by cu_seqlens.
+* :func:`prefill_backward` -- gradients of a left-padded batch's attention
+                              (q, k, v) for an upstream gradient of the output.
+* :func:`varlen_backward`  -- the same for packed documents.
 * :func:`decode_full`      -- the decode loop over a full-length cache that is
                               never compacted (positions 0 .. S+T-1).
 * :func:`decode_compact`   -- the same decode loop through the compact W+64
@@ -22,7 +25,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import attention, masks
+from . import attention, backward, masks
 from .compact import CompactModel, RingModel
 
 
@@ -62,6 +65,29 @@ def varlen_rows(q, k, v, cu_seqlens, window: int, scale: float, rows):
     doc = masks.doc_ids_from_cu_seqlens(cu_seqlens, total)
     m = masks.prefill_mask(total, window, 0, None, doc, rows=list(rows))
     return attention.masked_attention(_f64(q[list(rows)]), _f64(k), _f64(v), m, scale)
+
+
+def prefill_backward(q, k, v, dout, window: int, scale: float, valid_start=None, img=None):
+    """q, dout [B, S, Hq, D], k/v [B, S, Hkv, D] -> dq [B, S, Hq, D], dk, dv [B, S, Hkv, D]."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    b_count, s = q.shape[0], q.shape[1]
+    vs = np.zeros(b_count, dtype=np.int64) if valid_start is None else np.asarray(valid_start)
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    for b in range(b_count):
+        img_b = None if img is None else np.asarray(img[b])
+        m = masks.prefill_mask(s, window, int(vs[b]), img_b)
+        dq[b], dk[b], dv[b] = backward.masked_attention_backward(q[b], k[b], v[b], m, scale, dout[b])
+    return dq, dk, dv
+
+
+def varlen_backward(q, k, v, dout, cu_seqlens, window: int, scale: float):
+    """Packed documents: q, dout [T, Hq, D], k/v [T, Hkv, D] -> dq, dk, dv."""
+    total = k.shape[0]
+    doc = masks.doc_ids_from_cu_seqlens(cu_seqlens, total)
+    m = masks.prefill_mask(total, window, 0, None, doc)
+    return backward.masked_attention_backward(_f64(q), _f64(k), _f64(v), m, scale, _f64(dout))
 
 
 def decode_full(prompt_k, prompt_v, dec_q, dec_k, dec_v, prompt_len: int, window: int,
