@@ -63,3 +63,43 @@ def masked_attention_backward(q, k, v, mask, scale: float, do):
             dk[idx, h // g, :] += scale * np.outer(ds, q[i, h])
             dv[idx, h // g, :] += np.outer(p, do[i, h])
     return dq, dk, dv
+
+
+def masked_attention_backward_heads(q, k, v, mask, scale: float, do):
+    """The same gradients in matrix form, one query head at a time, for a
+    subset of query rows.
+
+    q, do [Sq, Hq, D] are the selected query rows, mask [Sq, Sk] their rows of
+    the mask, k, v [Sk, Hkv, D] every key.  Per head, with masked entries of P
+    zero: S = scale Q K^T, P = softmax over each row's allowed keys,
+    dP = dO V^T, delta = rowsum(P * dP), dS = P * (dP - delta),
+    dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.  Returns dq [Sq, Hq, D]
+    and the selected rows' contributions to dk, dv [Sk, Hkv, D]: exact for
+    every key that only the selected rows admit.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    hq = q.shape[1]
+    hkv = k.shape[1]
+    g = hq // hkv
+    mask = np.asarray(mask, dtype=bool)
+    live = mask.any(axis=1)
+    dq = np.zeros(q.shape, dtype=np.float64)
+    dk = np.zeros(k.shape, dtype=np.float64)
+    dv = np.zeros(v.shape, dtype=np.float64)
+    for h in range(hq):
+        kh, vh = k[:, h // g, :], v[:, h // g, :]
+        s = np.where(mask, scale * (q[:, h, :] @ kh.T), -np.inf)
+        m = np.where(live, s.max(axis=1), 0.0)
+        e = np.where(mask, np.exp(s - m[:, None]), 0.0)
+        tot = e.sum(axis=1)
+        p = e / np.where(live, tot, 1.0)[:, None]
+        dp = do[:, h, :] @ vh.T
+        delta = (p * dp).sum(axis=1)
+        ds = p * (dp - delta[:, None])
+        dq[:, h, :] = scale * (ds @ kh)
+        dk[:, h // g, :] += scale * (ds.T @ q[:, h, :])
+        dv[:, h // g, :] += p.T @ do[:, h, :]
+    return dq, dk, dv

@@ -13,6 +13,8 @@ compact-cache index model (``compact``):
 * :func:`prefill_backward` -- gradients of a left-padded batch's attention
                               (q, k, v) for an upstream gradient of the output.
 * :func:`varlen_backward`  -- the same for packed documents.
+* :func:`varlen_backward_rows` -- packed documents, selected query rows: their
+                              dq and their contributions to dk, dv.
 * :func:`decode_full`      -- the decode loop over a full-length cache that is
                               never compacted (positions 0 .. S+T-1).
 * :func:`decode_compact`   -- the same decode loop through the compact W+64
@@ -88,6 +90,17 @@ def varlen_backward(q, k, v, dout, cu_seqlens, window: int, scale: float):
     doc = masks.doc_ids_from_cu_seqlens(cu_seqlens, total)
     m = masks.prefill_mask(total, window, 0, None, doc)
     return backward.masked_attention_backward(_f64(q), _f64(k), _f64(v), m, scale, _f64(dout))
+
+
+def varlen_backward_rows(q, k, v, dout, cu_seqlens, window: int, scale: float, rows):
+    """Packed documents, selected query rows (matrix form per head): dq of
+    those rows [len(rows), Hq, D], and dk, dv [T, Hkv, D] summed over those
+    rows only -- exact for keys that no other query admits."""
+    total = k.shape[0]
+    rows = list(rows)
+    doc = masks.doc_ids_from_cu_seqlens(cu_seqlens, total)
+    m = masks.prefill_mask(total, window, 0, None, doc, rows=rows)
+    return backward.masked_attention_backward_heads(_f64(q[rows]), _f64(k), _f64(v), m, scale, _f64(dout[rows]))
 
 
 def decode_full(prompt_k, prompt_v, dec_q, dec_k, dec_v, prompt_len: int, window: int,

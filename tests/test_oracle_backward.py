@@ -15,7 +15,9 @@ against something that does not use those formulas:
   dv = the sum of the group's upstream gradients; pad rows and pad keys get
   zero gradients and pad rows' upstream gradients change nothing;
 * GQA: the Hkv-head gradients equal the repeated-K/V gradients summed over
-  each group; packed documents equal each document on its own, bit for bit.
+  each group; packed documents equal each document on its own, bit for bit;
+* the matrix form (one head at a time, optionally a subset of query rows)
+  equals the row-by-row form.
 """
 
 import numpy as np
@@ -139,3 +141,24 @@ def test_packed_documents_equal_each_document_alone():
         m = masks.prefill_mask(b - a, w)
         eq, ek, ev = backward.masked_attention_backward(q[a:b], k[a:b], v[a:b], m, 0.45, do[a:b])
         assert np.array_equal(dq[a:b], eq) and np.array_equal(dk[a:b], ek) and np.array_equal(dv[a:b], ev)
+
+
+def test_matrix_form_equals_row_form():
+    rng = np.random.default_rng(16)
+    n, hq, hkv, d, w = 70, 4, 2, 9, 12
+    q, k, v, do = _rand(rng, n, hq, d), _rand(rng, n, hkv, d), _rand(rng, n, hkv, d), _rand(rng, n, hq, d)
+    img = np.full(n, -1)
+    img[40:55] = 0
+    m = masks.prefill_mask(n, w, 6, img)
+    want = backward.masked_attention_backward(q, k, v, m, 0.35, do)
+    got = backward.masked_attention_backward_heads(q, k, v, m, 0.35, do)
+    for a, b in zip(want, got):
+        assert np.allclose(a, b, rtol=0, atol=1e-12)
+    # a subset of rows: exact dq for them, and exact dk / dv for the keys only
+    # they admit (the last 5 keys are admitted only by the last 5 queries here)
+    rows = list(range(n - 5, n))
+    gq, gk, gv = backward.masked_attention_backward_heads(q[rows], k, v, m[rows], 0.35, do[rows])
+    assert np.allclose(gq, want[0][rows], rtol=0, atol=1e-12)
+    assert not m[:n - 5, n - 5:].any()
+    assert np.allclose(gk[n - 5:], want[1][n - 5:], rtol=0, atol=1e-12)
+    assert np.allclose(gv[n - 5:], want[2][n - 5:], rtol=0, atol=1e-12)
