@@ -248,6 +248,46 @@ SWA_API swa_status swa_prefill(swa_cache* cache, int32_t layer, int32_t mode, in
                                const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, float scale,
                                swa_bf16* out, float* lse, swa_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Backward (training)                                                       */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes swa_prefill_backward needs for this meta (whole sequences:
+ * chunk_start = 0, chunk_len = seq_len) and head count; 0 with
+ * swa_last_error set on invalid arguments.  The score tiles dominate it:
+ * 3 x 32 KB per (sequence, query head, 128-row query tile, key tile of its
+ * band), the band being 1 + ceil((W - 1) / 128) key tiles without images and
+ * every key tile with them. */
+SWA_API size_t swa_prefill_backward_workspace_bytes(int32_t q_heads, const swa_prefill_meta* meta);
+
+/* Gradients of swa_prefill's output with respect to q, k and v, for training
+ * ("Add SDPA attention implementation", Summary: models with head size 512
+ * must train; its benchmark table times forward + backward of packed
+ * documents).  With P the softmax weights of the forward pass over the keys
+ * each query admits, dout = dL/dout, and delta_i = dout_i . out_i:
+ *   dv_j = sum_i P_ij dout_i,   dS_ij = scale * P_ij * (dout_i . v_j - delta_i),
+ *   dq_i = sum_j dS_ij k_j,     dk_j = sum_i dS_ij q_i,
+ * with dk and dv summed over the query heads that share a KV head.
+ * Whole sequences only (meta->chunk_start = 0, chunk_len = seq_len), with the
+ * plan swa_build_mask(SWA_MASK_PREFILL) built for that meta (padding, image
+ * blocks or packed documents as in swa_prefill's generic mode).
+ * Layouts: q, out, dout, dq [B, S, Hq, D]; k, v, dk, dv [B, S, Hkv, D]
+ * (packed documents: B = 1, S = T); lse [B, S, Hq] fp32 as swa_prefill wrote
+ * it (natural log); out is swa_prefill's output.  All bf16 except lse.
+ * Rows with no admitted key, and keys no query admits, get zero gradients.
+ * workspace: >= swa_prefill_backward_workspace_bytes device bytes, 256-byte
+ * aligned, no initialisation needed; the caller owns it.  Three kernels run
+ * on `stream`; calls that overlap on the GPU need separate workspaces.
+ * A device-side inconsistency (a band wider than the workspace allows, a
+ * bounded wait that gave up) is recorded in the plan's error word:
+ * swa_plan_check reports it.
+ * Supported: head_dim 256 or 512, Hq a multiple of Hkv. */
+SWA_API swa_status swa_prefill_backward(int32_t q_heads, int32_t kv_heads, int32_t head_dim,
+                                        const swa_prefill_meta* meta, const swa_bf16* q, const swa_bf16* k,
+                                        const swa_bf16* v, const swa_bf16* out, const swa_bf16* dout,
+                                        const float* lse, float scale, swa_bf16* dq, swa_bf16* dk,
+                                        swa_bf16* dv, void* workspace, size_t ws_bytes, swa_stream_t stream);
+
 /* Compaction at first decode ([SPYRE] Summary): rows [S - W, S) of every
  * (layer, sequence, head) slab of the prefill cache go to rows [0, W) of the
  * compact cache (same shape apart from rows, same S and W); rows of negative

@@ -164,6 +164,16 @@ bool check_meta(const swa_prefill_meta* m) {
   return true;
 }
 
+// Meta accepted by the backward pass: whole sequences and a plan.  Returns
+// SWA_OK or the failing status (g_error set).
+swa_status check_backward_meta(const swa_prefill_meta* meta) {
+  if (!check_meta(meta)) return SWA_EINVAL;
+  if (meta->chunk_start != 0 || meta->chunk_len != meta->seq_len)
+    return fail(SWA_EUNSUPPORTED, "backward covers whole sequences (chunk_start 0, chunk_len = seq_len)");
+  if (!meta->plan) return fail(SWA_EINVAL, "backward needs meta->plan (swa_build_mask(SWA_MASK_PREFILL))");
+  return SWA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -437,6 +447,65 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
   }
   cudaError_t e = swa::launch_prefill_tc(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  return SWA_OK;
+}
+
+size_t swa_prefill_backward_workspace_bytes(int32_t q_heads, const swa_prefill_meta* meta) {
+  if (check_backward_meta(meta) != SWA_OK) return 0;
+  if (q_heads < 1) {
+    fail(SWA_EINVAL, "q_heads must be >= 1");
+    return 0;
+  }
+  return swa::backward_layout(meta->batch, meta->seq_len, q_heads, meta->window, meta->img_id != nullptr).total;
+}
+
+swa_status swa_prefill_backward(int32_t q_heads, int32_t kv_heads, int32_t head_dim, const swa_prefill_meta* meta,
+                                const swa_bf16* q, const swa_bf16* k, const swa_bf16* v, const swa_bf16* out,
+                                const swa_bf16* dout, const float* lse, float scale, swa_bf16* dq, swa_bf16* dk,
+                                swa_bf16* dv, void* workspace, size_t ws_bytes, swa_stream_t stream) {
+  const swa_status ms = check_backward_meta(meta);
+  if (ms != SWA_OK) return ms;
+  if (q_heads < 1 || kv_heads < 1 || q_heads % kv_heads)
+    return fail(SWA_EINVAL, "q_heads must be a positive multiple of kv_heads");
+  if (head_dim != 256 && head_dim != 512) return fail(SWA_EUNSUPPORTED, "backward supports head_dim 256 and 512");
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace)
+    return fail(SWA_EINVAL, "q, k, v, out, dout, lse, dq, dk, dv and workspace are required");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3))
+    return fail(SWA_EINVAL, "tensor pointers must be 16-byte aligned (lse 4-byte)");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return fail(SWA_EINVAL, "workspace must be 256-byte aligned");
+  if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
+  const swa::BackwardLayout L =
+      swa::backward_layout(meta->batch, meta->seq_len, q_heads, meta->window, meta->img_id != nullptr);
+  if (ws_bytes < L.total)
+    return fail(SWA_EINVAL, "workspace too small: %zu bytes, need %zu", ws_bytes, L.total);
+  char* ws = static_cast<char*>(workspace);
+  swa::BackwardArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.plan = meta->plan;
+  a.delta = reinterpret_cast<float*>(ws + L.off_delta);
+  a.t_ds = ws + L.off_ds;
+  a.t_pt = ws + L.off_pt;
+  a.t_dst = ws + L.off_dst;
+  a.batch = meta->batch;
+  a.seq_len = meta->seq_len;
+  a.q_heads = q_heads;
+  a.kv_heads = kv_heads;
+  a.head_dim = head_dim;
+  a.band = L.band;
+  a.scale = scale;
+  a.err = reinterpret_cast<int32_t*>(const_cast<void*>(meta->plan)) + offsetof(swa::PlanHeader, error) / 4;
+  cudaError_t e = swa::launch_prefill_backward(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return SWA_OK;
 }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the CUDA translation units of libswa.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -17,6 +18,7 @@ enum DevError : int32_t {
   kErrImageCrossesChunk = 3, // an image block runs past the chunk end
   kErrBadDocs = 4,           // cu_seqlens does not cover the query rows
   kErrTimeout = 5,           // a bounded wait inside a kernel gave up
+  kErrBand = 6,              // a query tile's key tiles exceed the backward workspace band
 };
 
 // Query rows per prefill tile; the plan's per-tile key ranges use it.
@@ -151,5 +153,54 @@ struct PrefillArgs {
 
 // Tensor-core (tcgen05) prefill: head size 256 in one CTA, 512 in a CTA pair.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
+
+// 4-D bf16 tensor map with a {64, box_rows, 1, 1} box and 128-byte swizzle
+// (dims innermost first, strides in bytes of dims 1..3); false on failure.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    uint32_t box_rows);
+
+// ---------------------------------------------------------------- backward
+// Score tiles of the backward pass are 128 queries x 128 keys (the plan's
+// query tile); each is stored as the 128-byte-swizzled image of two
+// {64 columns, 128 rows} boxes (32 KB).
+constexpr int kBwdTile = 128;
+constexpr size_t kBwdTileBytes = size_t(kBwdTile) * kBwdTile * 2;
+
+struct BackwardLayout {
+  int n_tiles;       // query (= key) tiles per sequence: ceil(S / 128)
+  int band;          // key tiles reserved per query tile
+  size_t off_delta;  // [B, S, Hq] fp32: rowsum(dout * out)
+  size_t off_ds;     // dS tiles   [B, Hq, n_tiles, band] (rows: queries, columns: keys)
+  size_t off_pt;     // P^T tiles  (rows: keys, columns: queries)
+  size_t off_dst;    // dS^T tiles
+  size_t total;
+};
+// band = n_tiles when image blocks are present (future keys up to the block
+// end), else the most 128-key tiles a 128-row query tile can span under a
+// window of `window` keys: 1 + ceil((window - 1) / 128), capped at n_tiles.
+BackwardLayout backward_layout(int batch, int seq_len, int q_heads, int window, bool images);
+
+struct BackwardArgs {
+  const uint16_t* q;     // [B, S, Hq, D]
+  const uint16_t* k;     // [B, S, Hkv, D]
+  const uint16_t* v;
+  const uint16_t* out;   // forward output [B, S, Hq, D]
+  const uint16_t* dout;  // upstream gradient of out
+  const float* lse;      // forward lse [B, S, Hq]
+  uint16_t* dq;          // [B, S, Hq, D]
+  uint16_t* dk;          // [B, S, Hkv, D]
+  uint16_t* dv;
+  const void* plan;      // prefill plan of the whole sequences
+  float* delta;          // workspace parts (BackwardLayout)
+  char* t_ds;
+  char* t_pt;
+  char* t_dst;
+  int batch, seq_len, q_heads, kv_heads, head_dim, band;
+  float scale;
+  int32_t* err;          // plan header error word
+};
+
+// Three launches on `s`: delta, scores (P and dS tiles), gradients (dQ, dK, dV).
+cudaError_t launch_prefill_backward(const BackwardArgs& a, cudaStream_t s);
 
 }  // namespace swa

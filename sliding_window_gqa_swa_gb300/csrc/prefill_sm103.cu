@@ -776,33 +776,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 4-D bf16 tensor map with a {64, rows, 1, 1} box and 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
-              uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint32_t box[4] = {64, box_rows, 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <bool kPair, bool kSm2, bool kWide>
 cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
                         cudaStream_t s) {
@@ -835,6 +808,32 @@ cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
 
 }  // namespace
 
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], const uint64_t strides_bytes[3],
+                    uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t box[4] = {64, box_rows, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   const uint64_t D = uint64_t(a.head_dim);
@@ -846,12 +845,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
   const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
-  if (!make_map(&mk, a.k, kd, ks, sm2 ? BN / 2 : BN) || !make_map(&mv, a.v, kd, ks, BN)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&mk, a.k, kd, ks, sm2 ? BN / 2 : BN) || !make_tmap_bf16(&mv, a.v, kd, ks, BN))
+    return cudaErrorInvalidValue;
   // Q [B, C, Hq, D]: dims {D, C, Hq, B} (tiles of 128 rows; the pair kernel
   // loads them with TMA, the others read rows with 16-byte loads)
   const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
   const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
-  if (!make_map(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
   if (a.head_dim == 512)
     return sm2 ? launch_kind<false, true, true>(mq, mk, mv, a, s) : launch_kind<true, false, false>(mq, mk, mv, a, s);
   return sm2 ? launch_kind<false, true, false>(mq, mk, mv, a, s) : launch_kind<false, false, false>(mq, mk, mv, a, s);

@@ -67,6 +67,9 @@ _SIGS = {
     "swa_build_mask": (_I, [_P, _I, ctypes.POINTER(PrefillMeta), _P, _P]),
     "swa_plan_check": (_I, [_P, _P]),
     "swa_prefill": (_I, [_P, _I, _I, _I, _I, _I, ctypes.POINTER(PrefillMeta), _P, _P, _P, _F, _P, _P, _P]),
+    "swa_prefill_backward_workspace_bytes": (_SZ, [_I, ctypes.POINTER(PrefillMeta)]),
+    "swa_prefill_backward": (_I, [_I, _I, _I, ctypes.POINTER(PrefillMeta), _P, _P, _P, _P, _P, _P, _F, _P, _P, _P,
+                                  _P, _SZ, _P]),
     "swa_compact": (_I, [_P, _P, _P]),
     "swa_decode_workspace_bytes": (_SZ, [_P, _I]),
     "swa_decode": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
@@ -271,6 +274,30 @@ def prefill(cache: Optional[Cache], layer: int, mode: int, q: torch.Tensor, k: O
     check(_lib.swa_prefill(cache.handle if cache else None, layer, mode, hq, kv_heads, d, ctypes.byref(meta.c),
                            ptr(q), ptr(k), ptr(v), float(scale), ptr(out), ptr(lse), stream_handle(stream)),
           "swa_prefill")
+
+
+def backward_workspace_bytes(q_heads: int, meta: Meta) -> int:
+    n = int(_lib.swa_prefill_backward_workspace_bytes(q_heads, ctypes.byref(meta.c)))
+    if n == 0:
+        raise SwaError(EINVAL, f"swa_prefill_backward_workspace_bytes: {last_error()}")
+    return n
+
+
+def backward_workspace(q_heads: int, meta: Meta, device=None) -> torch.Tensor:
+    """A workspace for swa_prefill_backward (no initialisation needed)."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    return torch.empty(backward_workspace_bytes(q_heads, meta), dtype=torch.uint8, device=dev)
+
+
+def prefill_backward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, dout: torch.Tensor,
+                     lse: torch.Tensor, meta: Meta, scale: float, dq: torch.Tensor, dk: torch.Tensor,
+                     dv: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _bf16(t, n)
+    hq, hkv, d = q.shape[-2], k.shape[-2], q.shape[-1]
+    check(_lib.swa_prefill_backward(hq, hkv, d, ctypes.byref(meta.c), ptr(q), ptr(k), ptr(v), ptr(out), ptr(dout),
+                                    ptr(lse), float(scale), ptr(dq), ptr(dk), ptr(dv), ptr(workspace),
+                                    workspace.numel(), stream_handle(stream)), "swa_prefill_backward")
 
 
 def compact(prefill_cache: Cache, compact_cache: Cache, stream=None) -> None:

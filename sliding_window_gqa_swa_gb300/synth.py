@@ -25,6 +25,10 @@ Recipe (seed = 1000 + workload number, draws in the order listed):
 5. packed varlen forward: 4 documents of 4096 tokens (T=16384), Hq=16, Hkv=8,
    D=512, W=4096; q, k ~ N(0, std 1/sqrt(D)), v ~ N(0,1).
 
+Backward (training) cases add an upstream gradient dout ~ N(0,1) of the
+output's shape, drawn from its own generator (seed + 500) so the forward
+inputs stay the same draws.
+
 Normal draws are float32 ``torch.randn`` rounded to bf16 (round to nearest
 even).  The same generators build smaller cases for the parity tests.
 """
@@ -205,6 +209,11 @@ def varlen_case(seed: int, *, doc_lens, q_heads: int, kv_heads: int, head_dim: i
     for n in doc_lens:
         cu.append(cu[-1] + int(n))
     return VarlenCase(q_heads, kv_heads, head_dim, window, q, k, v, torch.tensor(cu, dtype=torch.int32))
+
+
+def upstream_grad(seed: int, shape) -> torch.Tensor:
+    """dL/dout for a backward case: N(0,1) in bf16 from generator seed + 500."""
+    return _normal(torch.Generator().manual_seed(seed + 500), shape)
 
 
 def workload5() -> VarlenCase:

@@ -111,3 +111,42 @@ def test_prefill_meta_validation(swa):
     # packed documents with padding are unsupported
     m2 = swa.PrefillMeta(1, 100, 0, 100, 16, 2, fake, None, ctypes.c_void_p(0x20000), None)
     assert lib.swa_prefill_plan_bytes(ctypes.byref(m2)) == 0
+
+
+def test_backward_workspace_and_validation(swa):
+    lib = swa.lib()
+    fake = ctypes.c_void_p(0x10000)
+    plan = ctypes.c_void_p(0x40000)
+    # packed documents 4 x 4096, W = 4096: 128 query tiles, a band of 1 + 32 key tiles
+    cu = ctypes.c_void_p(0x20000)
+    m = swa.PrefillMeta(1, 16384, 0, 16384, 4096, 4, None, None, cu, plan)
+    n = lib.swa_prefill_backward_workspace_bytes(16, ctypes.byref(m))
+    tiles = 16 * 128 * 33
+    assert n == 16384 * 16 * 4 + 3 * tiles * 32768
+    # a window of 1 key: one key tile per query tile; images: every key tile (the
+    # delta array, 2 x 300 x 4 fp32, is rounded up to 256 bytes: 9728)
+    m1 = swa.PrefillMeta(2, 300, 0, 300, 1, 0, None, None, None, plan)
+    assert lib.swa_prefill_backward_workspace_bytes(4, ctypes.byref(m1)) == 9728 + 3 * 2 * 4 * 3 * 32768
+    mi = swa.PrefillMeta(2, 300, 0, 300, 1, 0, None, ctypes.c_void_p(0x30000), None, plan)
+    assert lib.swa_prefill_backward_workspace_bytes(4, ctypes.byref(mi)) == 9728 + 3 * 2 * 4 * 9 * 32768
+    # chunks and a missing plan are rejected
+    mc = swa.PrefillMeta(1, 300, 0, 200, 64, 0, None, None, None, plan)
+    assert lib.swa_prefill_backward_workspace_bytes(4, ctypes.byref(mc)) == 0
+    mp = swa.PrefillMeta(1, 300, 0, 300, 64, 0, None, None, None, None)
+    assert lib.swa_prefill_backward_workspace_bytes(4, ctypes.byref(mp)) == 0
+    assert "plan" in swa.last_error()
+
+    def call(meta, hq=4, hkv=2, d=256, ws=fake, ws_bytes=1 << 40, lse=fake):
+        return lib.swa_prefill_backward(hq, hkv, d, ctypes.byref(meta), fake, fake, fake, fake, fake, lse, 0.1,
+                                        fake, fake, fake, ws, ws_bytes, None)
+
+    m2 = swa.PrefillMeta(1, 300, 0, 300, 64, 0, None, None, None, plan)
+    assert call(mc) == swa.EUNSUPPORTED
+    assert call(mp) == swa.EINVAL
+    assert call(m2, d=128) == swa.EUNSUPPORTED
+    assert call(m2, hq=3) == swa.EINVAL
+    assert call(m2, lse=None) == swa.EINVAL
+    assert call(m2, ws=ctypes.c_void_p(0x10000 + 16)) == swa.EINVAL
+    assert "256-byte" in swa.last_error()
+    assert call(m2, ws_bytes=1000) == swa.EINVAL
+    assert "workspace too small" in swa.last_error()
