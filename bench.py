@@ -13,7 +13,8 @@ Headline: decode microseconds per layer (lower is better) = decode-phase
 device time / (512 steps x 26 layers).  The same line carries prefill
 TFLOP/s, the roofline of the dominant kernel, an end-to-end variant through
 pinned host buffers, the CPU oracle baseline, and secondary workloads
-(batched decode GB/s, chunked VLM prefill and packed-document prefill TFLOP/s).
+(batched decode GB/s, chunked VLM prefill and packed-document prefill TFLOP/s,
+and the packed-document training step: forward + backward TFLOP/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -334,7 +335,7 @@ def run_ours(args):
         del ejob
         torch.cuda.empty_cache()
 
-    secondary = {} if args.no_secondary else run_secondary(swa, synth, dev, peaks)
+    secondary = {} if args.no_secondary else run_secondary(swa, synth, dev, peaks, args.training_docs)
     if not args.no_secondary:
         # the same job through the modular ring cache (W rows, no roll)
         rjob = SingleStreamJob(swa, case, dev, ring=True)
@@ -420,10 +421,11 @@ def run_ours(args):
 
 
 # ----------------------------------------------------------------------------- secondary workloads
-def run_secondary(swa, synth, dev, peaks):
+def run_secondary(swa, synth, dev, peaks, training_docs=4):
     out = {}
     for name, fn in (("batched_decode", bench_batched_decode), ("chunked_vlm_prefill", bench_vlm_prefill),
-                     ("packed_prefill_d512", bench_packed)):
+                     ("packed_prefill_d512", bench_packed),
+                     ("packed_training_d512", lambda *a: bench_training(*a, docs=training_docs))):
         try:
             out[name] = fn(swa, synth, dev, peaks)
         except Exception as e:  # reported in the line, never hidden
@@ -562,6 +564,54 @@ def bench_packed(swa, synth, dev, peaks):
             "ms": round(ms, 3), "tflops": round(tf, 2), "tensor_frac": round(tf / peaks["bf16_tflops"], 4)}
 
 
+# Forward + backward of one packed 16K-token batch (4 x 4096) at head size 512, 16/8
+# heads, as the Fast-LLM page times it on H100 (sdpa-nested, bf16, fwd+bwd wall)
+FASTLLM_H100_FWD_BWD_MS = 88.0
+
+
+def bench_training(swa, synth, dev, peaks, docs=4):
+    """Training step of the packed workload: plan + forward (out, lse) + backward
+    (dq, dk, dv for an N(0,1) upstream gradient); best of 3 after one warm-up.
+    ``docs`` < 4 packs fewer 4096-token documents (a smaller case for profiling)."""
+    c = synth.workload5() if docs == 4 else synth.varlen_case(
+        synth.SEED_BASE + 5, doc_lens=[4096] * docs, q_heads=16, kv_heads=8, head_dim=512, window=4096)
+    T = int(c.cu_seqlens[-1])
+    Hq, D, W = c.q_heads, c.head_dim, c.window
+    meta = swa.Meta(1, T, 0, T, W, cu_seqlens=c.cu_seqlens.to(dev))
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    g = synth.upstream_grad(synth.SEED_BASE + 5, c.q.shape).to(dev)
+    o = torch.empty(T, Hq, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, Hq, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    swa.build_prefill_plan(meta)
+    ws = swa.backward_workspace(Hq, meta, device=dev)
+
+    def run():
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record()
+        swa.build_prefill_plan(meta, out=meta.plan)
+        swa.prefill(None, 0, swa.MODE_GENERIC, q, k, v, meta, D ** -0.5, o, lse)
+        e1.record()
+        swa.prefill_backward(q, k, v, o, g, lse, meta, D ** -0.5, dq, dk, dv, ws)
+        e2.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), e1.elapsed_time(e2)
+
+    run()
+    fwd_ms, bwd_ms = min((run() for _ in range(3)), key=lambda t: t[0] + t[1])
+    pairs = docs * causal_pairs(4096, W)
+    fwd_flop, bwd_flop = 4.0 * D * Hq * pairs, 10.0 * D * Hq * pairs
+    tf = (fwd_flop + bwd_flop) / ((fwd_ms + bwd_ms) * 1e-3) / 1e12
+    bwd_tf = bwd_flop / (bwd_ms * 1e-3) / 1e12
+    return {"workload": f"training step of packed documents {docs} x 4096, Hq=16 Hkv=8 D=512 W=4096: forward + "
+                        "backward",
+            "fwd_ms": round(fwd_ms, 3), "bwd_ms": round(bwd_ms, 3), "fwd_bwd_ms": round(fwd_ms + bwd_ms, 3),
+            "tflops": round(tf, 2), "bwd_tflops": round(bwd_tf, 2), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
+            "flop": "forward 4 D Hq pairs, backward 10 D Hq pairs (QK^T, dO V^T, dV, dK, dQ)",
+            "workspace_gb": round(ws.numel() / 1e9, 2),
+            "context_h100_sdpa_nested_fwd_bwd_ms": FASTLLM_H100_FWD_BWD_MS}
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def _oracle_decode_queries(case, n_queries, first=0):
     """Run the fp64 oracle on ``n_queries`` (step, layer) decode queries."""
@@ -627,6 +677,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-queries", type=int, default=104)
+    ap.add_argument("--training-docs", type=int, default=4, choices=[1, 2, 3, 4],
+                    help="4096-token documents in the training-step secondary line (4 = the full workload)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -203,7 +203,9 @@ scores_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   int32_t* err = a.err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x, qt = blockIdx.y, b = blockIdx.z;
+  // the last query tiles of a causal sequence have the most key tiles: they are
+  // scheduled first, so the short ones fill the tail of the grid
+  const int h = blockIdx.x, qt = int(gridDim.y - 1 - blockIdx.y), b = blockIdx.z;
   const int hk = h / (a.q_heads / a.kv_heads);
   const int nqt = (a.seq_len + BT - 1) / BT;
   const PlanLayout L = plan_layout(a.batch, a.seq_len);
@@ -361,13 +363,20 @@ scores_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int u = 0; u < 4; ++u)
           *reinterpret_cast<uint4*>(ds_tile + tile_off(r, col + 8 * u)) =
               make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
-        // P^T and dS^T: row = key, column r
+        // P^T and dS^T: row = key, column r.  Lanes r and r + 1 (r even) hold
+        // the two halves of one 4-byte word of each row: per pair of keys
+        // (c, c + 1) the even lane stores row c and the odd lane row c + 1,
+        // after one exchange of the half each needs
+        const bool odd = lane & 1;
+        const int r0 = r & ~1;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const uint32_t off = tile_off(col + e, r);
-          const uint32_t pwv = pw[e >> 1], dwv = dw[e >> 1];
-          *reinterpret_cast<uint16_t*>(pt_tile + off) = uint16_t((e & 1) ? (pwv >> 16) : (pwv & 0xffffu));
-          *reinterpret_cast<uint16_t*>(dst_tile + off) = uint16_t((e & 1) ? (dwv >> 16) : (dwv & 0xffffu));
+        for (int e = 0; e < 32; e += 2) {
+          const uint32_t pwv = pw[e >> 1], dwv = dw[e >> 1];  // lo: key col + e, hi: key col + e + 1
+          const uint32_t px = __shfl_xor_sync(0xffffffffu, odd ? (pwv & 0xffffu) : (pwv >> 16), 1);
+          const uint32_t dx = __shfl_xor_sync(0xffffffffu, odd ? (dwv & 0xffffu) : (dwv >> 16), 1);
+          const uint32_t off = tile_off(col + e + (odd ? 1 : 0), r0);
+          *reinterpret_cast<uint32_t*>(pt_tile + off) = odd ? (px | (pwv & 0xffff0000u)) : ((pwv & 0xffffu) | (px << 16));
+          *reinterpret_cast<uint32_t*>(dst_tile + off) = odd ? (dx | (dwv & 0xffff0000u)) : ((dwv & 0xffffu) | (dx << 16));
         }
       }
     }
@@ -408,6 +417,9 @@ __device__ __forceinline__ GradJob grad_job(const BackwardArgs& a, int nqt) {
   j.half = int(x % halves);
   x /= halves;
   j.tile = int(x % nqt);
+  // dQ: the last query tiles have the widest bands, so they go first (dV / dK:
+  // the first key tiles are admitted by the most query tiles and already lead)
+  if (j.kind == 2) j.tile = nqt - 1 - j.tile;
   x /= nqt;
   const int heads = j.kind == 2 ? a.q_heads : a.kv_heads;
   j.head = int(x % heads);
