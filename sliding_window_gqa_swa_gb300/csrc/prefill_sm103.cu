@@ -214,7 +214,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int col0 = half * HS;
   const int hq = kPair ? int(blockIdx.x >> 1)
                        : (kWide ? 2 * int(blockIdx.x >> 2) + crank : int(blockIdx.x));
-  const int qt = blockIdx.y, b = blockIdx.z;
+  // query tiles late in a causal sequence or document have the most key tiles:
+  // they are scheduled first, so the short ones fill the tail of the grid
+  const int qt = int(gridDim.y - 1 - blockIdx.y), b = blockIdx.z;
   const int hk = hq / (a.q_heads / a.kv_heads);
   const int i0 = qt * BM;
   const int q0 = a.chunk_start + i0;
