@@ -1,7 +1,7 @@
 """Guard canaries: every buffer a kernel writes sits between two 4 KB guard
 zones filled with a byte pattern, which must be intact after the calls
-(out-of-bounds writes of prefill, compaction, decode, roll and the mask
-builders would show there).  This stands in for a memory checker, which this
+(out-of-bounds writes of prefill, compaction, decode, roll, the mask
+builders and the backward pass would show there).  This stands in for a memory checker, which this
 GPU pool does not run.
 """
 
@@ -108,3 +108,27 @@ def test_decode_compact_roll_writes_stay_inside(swa):
         torch.cuda.synchronize()
         cmp_.check()
     assert all(g.intact() for g in guards)
+
+
+@pytest.mark.parametrize("docs,hq,hkv,d,w", [([300, 70], 4, 2, 512, 200), ([129, 1, 130], 3, 1, 256, 64)])
+def test_backward_writes_stay_inside(swa, docs, hq, hkv, d, w):
+    dev = torch.device("cuda")
+    c = synth.varlen_case(4500 + d, doc_lens=docs, q_heads=hq, kv_heads=hkv, head_dim=d, window=w)
+    T = int(c.cu_seqlens[-1])
+    meta = swa.Meta(1, T, 0, T, w, cu_seqlens=c.cu_seqlens.to(dev))
+    gp = Guarded(meta.plan_bytes())
+    swa.build_prefill_plan(meta, out=gp.mem)
+    q, k, v = c.q.to(dev), c.k.to(dev), c.v.to(dev)
+    g = synth.upstream_grad(4500 + d, c.q.shape).to(dev)
+    out = torch.empty(T, hq, d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(T, hq, dtype=torch.float32, device=dev)
+    swa.prefill(None, 0, swa.MODE_GENERIC, q, k, v, meta, d ** -0.5, out, lse)
+    gq = Guarded(_nbytes((T, hq, d), torch.bfloat16))
+    gk = Guarded(_nbytes((T, hkv, d), torch.bfloat16))
+    gv = Guarded(_nbytes((T, hkv, d), torch.bfloat16))
+    gw = Guarded(swa.backward_workspace_bytes(hq, meta))
+    swa.prefill_backward(q, k, v, out, g, lse, meta, d ** -0.5, gq.view(torch.bfloat16, (T, hq, d)),
+                         gk.view(torch.bfloat16, (T, hkv, d)), gv.view(torch.bfloat16, (T, hkv, d)), gw.mem)
+    torch.cuda.synchronize()
+    swa.plan_check(gp.mem)
+    assert all(x.intact() for x in (gp, gq, gk, gv, gw))
