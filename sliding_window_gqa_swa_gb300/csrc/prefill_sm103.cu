@@ -838,6 +838,7 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], co
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
+  if (a.head_dim == 256) return launch_prefill_t128(a, s);
   const uint64_t D = uint64_t(a.head_dim);
   CUtensorMap mq, mk, mv;
   // query heads 2g and 2g + 1 share a KV head when the group size is even:
