@@ -1,25 +1,28 @@
-// Prefill attention on the 5th-generation tensor cores (tcgen05).
+// Prefill attention on the 5th-generation tensor cores (tcgen05) on 64-key
+// tiles, for head size 512 (head size 256 runs prefill128_kernel).
 //
 // One CTA computes 128 query rows of one query head, over a 256-column slice
 // of the head dimension, against the key tiles (64 keys each) its rows need;
 // the tile range comes from the causal arithmetic or from the plan built on
-// the device (generic plan: image blocks, documents).  Three shapes:
-//   * head size 256, even GQA group (kSm2): the two CTAs of a cluster are
+// the device (generic plan: image blocks, documents).  The template holds
+// three shapes; launch_prefill_tc dispatches the two head-size-512 ones:
+//   * head pair (kSm2, kWide: even GQA group): the two CTAs of a cluster are
 //     query heads 2g and 2g + 1 of one KV head and share every MMA
 //     (cta_group::2, M = 256).  Each CTA loads half of every K tile (32 keys)
 //     and half of every V tile (128 head-dimension columns).  Tensor memory
-//     per CTA: O (256 columns), three S buffers (64 each), two P buffers (32
-//     each, bf16 pairs; P is the A operand of PV from tensor memory); Q stays
-//     in shared memory;
-//   * head size 256, odd group: one CTA per head (cta_group::1); tensor
-//     memory holds O, two S buffers and the Q slice (128 columns, the A
-//     operand of QK^T); P goes through shared memory;
-//   * head size 512 (kPair): the two CTAs of a cluster hold the two 256-column
-//     halves of the head; each computes a partial S over its half of the
-//     contraction and sends it into one of the peer's two exchange buffers
-//     with asynchronous remote stores; both add the two partials (fp32
-//     addition commutes: the same S bit for bit), run the identical softmax,
-//     and accumulate their own half of O -- no MMA is done twice.
+//     per CTA: O (256 columns of one column half; consecutive clusters take
+//     the two halves and both compute S over the whole contraction) and two S
+//     buffers, each the lo and hi partials of two MMA chains over the halves
+//     of the contraction; P (bf16 pairs) overwrites its S columns and is the
+//     A operand of PV from tensor memory; Q stays in shared memory;
+//   * column pair (kPair: odd group): the two CTAs of a cluster hold the two
+//     256-column halves of the head; each computes a partial S over its half
+//     of the contraction and sends it into one of the peer's two exchange
+//     buffers with asynchronous remote stores; both add the two partials
+//     (fp32 addition commutes: the same S bit for bit), run the identical
+//     softmax, and accumulate their own half of O -- no MMA is done twice;
+//   * single CTA (neither; head size 256, no longer dispatched): Q slice and
+//     two S buffers in tensor memory, P through shared memory.
 // Warp roles:
 //   warp 0     TMA producer: K and V slices into a ring of slots (128-byte
 //              swizzled, 64-column boxes), in the order the MMA thread
