@@ -534,9 +534,32 @@ def bench_vlm_prefill(swa, synth, dev, peaks):
     ms = min(run() for _ in range(3))
     pairs = sum(admitted_pairs(S, W, int(c.valid_start[b]), c.img_id[b].numpy()) for b in range(B))
     tf = 4.0 * D * Hq * pairs / (ms * 1e-3) / 1e12
+    executed = sum(executed_tile_pairs(meta.plan, B, C) for meta, *_ in chunks)
     return {"workload": "chunked prefill B=4 S=8192 (4 x 2048) Hq=8 Hkv=4 D=256 W=1024, image blocks",
             "ms": round(ms, 3), "tflops": round(tf, 2), "tensor_frac": round(tf / peaks["bf16_tflops"], 4),
-            "pairs_per_head": pairs, "includes": "plan build + K/V write + attention, 4 chunks"}
+            "pairs_per_head": pairs, "executed_pairs_per_head": executed,
+            "useful_frac": round(pairs / executed, 4) if executed else None,
+            "tiles": "128 query rows x 128 keys per executed tile (head size 256 kernel); a tile's key range "
+                     "is the plan's per-query-tile range",
+            "includes": "plan build + K/V write + attention, 4 chunks"}
+
+
+def executed_tile_pairs(plan, batch, chunk_len, bm=128, bn=128):
+    """(query, key) pairs the head-size-256 prefill computes for one chunk and head: for every
+    128-row query tile, the 128-key tiles spanning the plan's key range [klo, khi).  The plan
+    buffer is header (256 B) | row_lo [B, C] | row_hi [B, C] | tile_klo [B, T] | tile_khi [B, T],
+    int32, each part 256-byte aligned (T = ceil(C / 128))."""
+    def a256(x):
+        return (x + 255) & ~255
+    nqt = (chunk_len + bm - 1) // bm
+    raw = plan.cpu().numpy()
+    rows = a256(batch * chunk_len * 4)
+    off_tlo = 256 + 2 * rows
+    off_thi = off_tlo + a256(batch * nqt * 4)
+    klo = raw[off_tlo:off_tlo + batch * nqt * 4].view(np.int32).astype(np.int64)
+    khi = raw[off_thi:off_thi + batch * nqt * 4].view(np.int32).astype(np.int64)
+    n = np.where(khi > klo, (khi - 1) // bn - klo // bn + 1, 0)
+    return int(n.sum()) * bm * bn
 
 
 def bench_packed(swa, synth, dev, peaks):
