@@ -107,8 +107,8 @@ typedef struct swa_cache_desc {
 
 /* Device-side cache state (the first 32 bytes of the cache memory).  Kernels
  * read position data only from here, so one captured graph serves every
- * decode position ([SPYRE] Compilation behavior: position, origin and
- * padding travel only in tensor data). */
+ * decode position ([SPYRE] Compilation behavior: positions, the origin and
+ * padding are device data, not constants of the compiled program). */
 typedef struct swa_device_state {
   int32_t origin;     /* position held by row 0 (compact: S - W at first)   */
   int32_t next_row;   /* row the next decode step writes                    */
@@ -303,16 +303,16 @@ SWA_API swa_status swa_compact(const swa_cache* prefill, swa_cache* compact, swa
 SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_heads);
 
 /* One decode token of one sliding layer, after swa_build_mask(DECODE) of the
- * step: appends k_new, v_new [B, Hkv, D] at the step's row (decode writes go
- * through the compact cache index, [SPYRE] Summary), then attends q [B, Hq, D]
- * over the rows the mask [B, rows] admits (decode scans only the compact
- * allocation, [SPYRE] Compilation behavior).  Split-K over rows, with the last
+ * step: appends k_new, v_new [B, Hkv, D] at the step's row (the new row goes
+ * into the compact cache at its row index, [SPYRE] Summary), then attends
+ * q [B, Hq, D] over the rows the mask [B, rows] admits (decode reads only the
+ * compact buffer's rows, [SPYRE] Compilation behavior).  Split-K over rows, with the last
  * CTA of each (sequence, kv head) combining the partial results.
  * out [B, Hq, D] bf16; lse [B, Hq] fp32 or NULL.
  * workspace: >= swa_decode_workspace_bytes device bytes, zero-filled before
  * its first use; each call leaves it ready for the next.  Calls that overlap
  * on the GPU need separate workspaces.
- * KV-sharing layer ([SPYRE] Summary: KV-sharing behavior is preserved):
+ * KV-sharing layer ([SPYRE] Summary: layers that reuse another layer's K/V keep working):
  * k_new = v_new = NULL attends over layer `layer`'s rows without appending;
  * that layer's own swa_decode must already have appended this step's row.
  * Launch chaining: the kernel is launched with programmatic dependent launch.
@@ -355,8 +355,8 @@ SWA_API swa_status swa_decode_noalloc(swa_cache* cache, int32_t layer, int32_t q
                                       const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
                                       float scale, swa_bf16* out, float* lse, swa_stream_t stream);
 
-/* The roll every 64 decode tokens ([SPYRE] Summary: offset-aware
- * device-to-device copies): when next_row == rows, rows [64, rows) of every
+/* The roll every 64 decode tokens ([SPYRE] Summary: rows shift down by a
+ * fixed offset with device-to-device copies): when next_row == rows, rows [64, rows) of every
  * slab of every layer move to rows [0, W) (an overlap-safe in-place shift),
  * origin += 64, next_row = W.  SWA_ESTATE unless the roll is due (a ring
  * cache never rolls). */

@@ -3,8 +3,8 @@
 For a query row ``i`` and query head ``h`` the key/value head is
 ``h // G`` with ``G = Hq / Hkv``: each key/value head serves G consecutive
 query heads, which is what repeating K/V with ``repeat_interleave`` across the
-query heads computes ([FASTLLM] Summary: both SDPA paths repeat K/V across
-query heads).
+query heads computes ([FASTLLM] Summary: its SDPA paths copy every K/V head
+once per query head of its group).
 
     allowed keys  A_i = { k : mask[i, k] }            (in increasing k order)
     s_k  = scale * <q_ih, k_k>                         k in A_i

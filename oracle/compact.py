@@ -4,12 +4,12 @@ What the pages fix ([SPYRE] Summary and Compilation behavior):
   * prefill writes a prompt-sized sliding cache;
   * at first decode it is compacted into a bounded "window + 64" anchored
     buffer (the 1088-row allocation for W = 1024);
-  * decode writes go through the compact cache index;
-  * one fixed-shape runtime mask per decode step is shared by all sliding
-    layers; position, unwritten rows and window placement exist only as
-    tensor data;
-  * the compact cache is rolled every 64 decode tokens with offset-aware
-    device-to-device copies.
+  * each decode step's new row goes into the compact cache at its row index;
+  * one runtime mask of fixed shape per decode step serves every sliding
+    layer; positions, rows not yet written and where the window sits are
+    data, not constants;
+  * every 64 decode tokens the compact cache's rows shift down by a fixed
+    offset (device-to-device copies).
 
 Readings where the pages are silent:
   * anchoring is right-aligned: row r holds position origin + r with

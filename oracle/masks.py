@@ -10,8 +10,8 @@ position ``k`` of the same sequence:
                                                                 (causal OR same image)
 
 Sources:
-  * window AND (causal OR vision-blockwise) for sliding layers, global layers
-    stay causal: [SPYRE] Summary, the bullet on matching the Transformers VLM
+  * sliding layers admit a key inside the window that is causal or in the
+    query's image block, global layers stay causal: [SPYRE] Summary, the bullet on matching the Transformers VLM
     mask composition.
   * future same-image pairs are allowed, old same-image pairs outside the
     window are rejected: [SPYRE] Correctness, the mask-order regression bullet.

@@ -4,8 +4,8 @@
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
 // variants", Summary (prompt-sized caches compacted at first decode into
-// window + 64 anchored buffers; roll every 64 decode tokens with offset-aware
-// device-to-device copies).
+// window + 64 anchored buffers; every 64 decode tokens the rows shift down by
+// a fixed offset with device-to-device copies).
 
 #include "internal.h"
 

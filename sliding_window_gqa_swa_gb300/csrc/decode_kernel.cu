@@ -21,9 +21,9 @@
 // The merge order is fixed everywhere, so results are deterministic.
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
-// variants", Summary (decode writes through the compact cache index; one
-// runtime mask per step) and Compilation behavior (decode scans only the
-// compact 1088-row allocation); "Add SDPA attention implementation", Summary
+// variants", Summary (the step's new row goes into the compact cache at its
+// row index; one runtime mask per step) and Compilation behavior (decode
+// reads only the 1088 rows of the compact buffer); "Add SDPA attention implementation", Summary
 // (K/V shared by query-head groups).
 
 #include <cuda_bf16.h>

@@ -4,9 +4,10 @@
 //
 // Sources: "Enable compact sliding-window attention for Gemma 3 and Gemma 4
 // variants", Summary (one fixed-shape runtime mask shared by all sliding
-// layers; window AND (causal OR vision-blockwise)) and Compilation behavior
-// (position, unwritten rows, window placement, padding and VLM regions travel
-// only in tensor data); "Add SDPA attention implementation", Summary
+// layers; a key counts when it lies in the window and is causal or in the
+// query's image block) and Compilation behavior (positions, rows not yet
+// written, where the window sits, padding and image regions are device data,
+// not constants of the compiled program); "Add SDPA attention implementation", Summary
 // (document boundaries from cu_seqlens).
 
 #include "internal.h"

@@ -4,8 +4,9 @@
 * the runtime mask admits exactly the positions the full-length decode
   predicate admits, each once (no stale duplicate), at every step;
 * compact W+64 attention equals full-cache masked attention bit for bit at
-  every step of the 70-step anchored decode across a roll (the pages'
-  "anchored 70-step decode across a cache roll"), and over 512 steps of the
+  every step of a 70-step decode over the anchored buffer that crosses one
+  roll (the case the Spyre page's Correctness section checks), and over 512
+  steps of the
   single-stream shape;
 * pad rows and never-written rows get zero weight (bit-identical outputs
   after filling them with large finite values);
