@@ -4,8 +4,7 @@
 // One CTA computes 128 query rows of one query head, over a 256-column slice
 // of the head dimension, against the key tiles (64 keys each) its rows need;
 // the tile range comes from the causal arithmetic or from the plan built on
-// the device (generic plan: image blocks, documents).  The template holds
-// three shapes; launch_prefill_tc dispatches the two head-size-512 ones:
+// the device (generic plan: image blocks, documents).  Two shapes:
 //   * head pair (kSm2, kWide: even GQA group): the two CTAs of a cluster are
 //     query heads 2g and 2g + 1 of one KV head and share every MMA
 //     (cta_group::2, M = 256).  Each CTA loads half of every K tile (32 keys)
@@ -20,9 +19,7 @@
 //     of the contraction and sends it into one of the peer's two exchange
 //     buffers with asynchronous remote stores; both add the two partials
 //     (fp32 addition commutes: the same S bit for bit), run the identical
-//     softmax, and accumulate their own half of O -- no MMA is done twice;
-//   * single CTA (neither; head size 256, no longer dispatched): Q slice and
-//     two S buffers in tensor memory, P through shared memory.
+//     softmax, and accumulate their own half of O -- no MMA is done twice.
 // Warp roles:
 //   warp 0     TMA producer: K and V slices into a ring of slots (128-byte
 //              swizzled, 64-column boxes), in the order the MMA thread
@@ -90,7 +87,7 @@ struct Layout {
   static constexpr int Q_BYTES = Q_CHUNK * (HQK / 64);
   static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;    // one ring slot
   static constexpr int KSLOTS = kWide ? 2 : 1;                   // ring slots of one K tile
-  static constexpr int NST = kPair ? 4 : (kSm2 ? (kWide ? 6 : 10) : 6);  // ring slots
+  static constexpr int NST = kPair ? 4 : 6;                      // ring slots
   static constexpr int NS = 2;                                   // S buffers in TMEM
   static constexpr int SB = kSm2 ? 2 * BN : BN;                  // TMEM columns of one S buffer
   static constexpr int OFF_Q = 0;
@@ -106,7 +103,7 @@ struct Layout {
 };
 
 // TMEM columns: O, then the S buffers (TM_S + b * SB), then the Q slice when
-// it lives in tensor memory (single CTA: after two S buffers)
+// it lives in tensor memory (column pair: after two S buffers)
 constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
@@ -190,7 +187,8 @@ __global__ void __launch_bounds__(threads_of(kPair), 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
   using LY = Layout<kPair, kSm2, kWide>;
-  static_assert(!(kPair && kSm2) && (kSm2 || !kWide), "shape");
+  // head size 512: a head pair (kSm2 and kWide) or a column pair (kPair)
+  static_assert(kPair != kSm2 && kSm2 == kWide, "shape");
   constexpr int NST = LY::NST;
   constexpr int NS = LY::NS;
   constexpr int SB = LY::SB;
@@ -251,7 +249,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    // single CTA: the softmax threads copy Q into TMEM; kSm2: both CTAs' Q
+    // column pair: the softmax threads copy Q into TMEM; kSm2: both CTAs' Q
     // tiles complete on the issuing CTA's barrier
     mbar_init(bars.q(), kSm2 ? 1 : 256);
     for (int i = 0; i < 2; ++i) mbar_init(bars.s_full(i), 1);
@@ -573,24 +571,22 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // the unrounded ones (gives the lse)
     float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
     // The two warps of a row (one per group) meet at a named barrier for every
-    // tile in the pair kernels; a warp that gives up (timeout or abort) keeps
-    // meeting its partner there and skips the rest of each tile, so the
-    // barrier's arrivals stay paired and every role reaches the teardown.
-    constexpr bool kExchange = kPair || kSm2;
+    // tile; a warp that gives up (timeout or abort) keeps meeting its partner
+    // there and skips the rest of each tile, so the barrier's arrivals stay
+    // paired and every role reaches the teardown.
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const int sb = t % NS, pb = t & 1;
       if (ok) ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
-      if (!kExchange && !ok) break;
       if (ok) tc_fence_after();
       const uint32_t tS = tmem + lane_off + TM_S + sb * SB;
       const int k0 = (kt_lo + t) * BN;
       // the masking pass runs only when some row of the warp needs it
       const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
-      // sr[0, HC): this group's columns; single CTA: sr[HC, BN) the other group's
-      uint32_t sr[kExchange ? HC : BN];
+      // sr[0, HC): this group's columns
+      uint32_t sr[HC];
       float mraw = -CUDART_INF_F;
-      if constexpr (kExchange) {
+      {
         if (ok) {
           tmem_ld32(tS + cb, sr);
           if constexpr (kSm2) {
@@ -639,12 +635,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
         named_sync(bar_id);
         if (!ok) continue;
-      } else {
-        // both groups read the whole S row and take its maximum themselves
-        tmem_ld32(tS + cb, sr);
-        tmem_ld32(tS + (cb ^ HC), sr + HC);
-        tmem_ld_wait();
-        mraw = fmaxf(mask_max<HC>(sr, k0 + cb, lo, hi, masked), mask_max<HC>(sr + HC, k0 + (cb ^ HC), lo, hi, masked));
       }
       const float mt = mraw * c2;
       // lazy rescale: move the reference only when the maximum grows by > 2^8
@@ -652,10 +642,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
       if (__any_sync(0xffffffffu, rescale)) {
         ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
-        if (!ok) {
-          if constexpr (kExchange) continue;
-          else break;
-        }
+        if (!ok) continue;
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
         for (int c0 = grp * OC; c0 < grp * OC + OC; c0 += 32) {
@@ -698,10 +685,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       } else {
         if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
           ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
-          if (!ok) {
-            if constexpr (kExchange) continue;
-            else break;
-          }
+          if (!ok) continue;
         }
         uint8_t* prow = gbase + LY::OFF_P + pb * P_BYTES + r * 128;
 #pragma unroll
@@ -853,14 +837,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
   if (!make_tmap_bf16(&mk, a.k, kd, ks, sm2 ? BN / 2 : BN) || !make_tmap_bf16(&mv, a.v, kd, ks, BN))
     return cudaErrorInvalidValue;
-  // Q [B, C, Hq, D]: dims {D, C, Hq, B} (tiles of 128 rows; the pair kernel
-  // loads them with TMA, the others read rows with 16-byte loads)
+  // Q [B, C, Hq, D]: dims {D, C, Hq, B} (tiles of 128 rows; the head pair
+  // loads them with TMA, the column pair reads rows with 16-byte loads)
   const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
   const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
   if (!make_tmap_bf16(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
-  if (a.head_dim == 512)
-    return sm2 ? launch_kind<false, true, true>(mq, mk, mv, a, s) : launch_kind<true, false, false>(mq, mk, mv, a, s);
-  return sm2 ? launch_kind<false, true, false>(mq, mk, mv, a, s) : launch_kind<false, false, false>(mq, mk, mv, a, s);
+  // head size 512: a head pair for an even GQA group, a column pair otherwise
+  return sm2 ? launch_kind<false, true, true>(mq, mk, mv, a, s) : launch_kind<true, false, false>(mq, mk, mv, a, s);
 }
 
 }  // namespace swa
