@@ -150,3 +150,23 @@ def test_backward_workspace_and_validation(swa):
     assert "256-byte" in swa.last_error()
     assert call(m2, ws_bytes=1000) == swa.EINVAL
     assert "workspace too small" in swa.last_error()
+
+
+def test_degenerate_sizes_are_rejected_on_the_host(swa):
+    lib = swa.lib()
+    fake = ctypes.c_void_p(0x10000)
+    plan = ctypes.c_void_p(0x40000)
+    for b, s, c0, cl, w in [(1, 0, 0, 0, 16), (1, 100, 0, 0, 16), (0, 100, 0, 100, 16), (1, 100, 0, 100, 0),
+                            (1, 100, 100, 1, 16), (1, 100, -1, 10, 16)]:
+        m = swa.PrefillMeta(b, s, c0, cl, w, 0, None, None, None, plan)
+        assert lib.swa_prefill_plan_bytes(ctypes.byref(m)) == 0
+        assert lib.swa_prefill_backward_workspace_bytes(4, ctypes.byref(m)) == 0
+        assert lib.swa_prefill(None, 0, swa.MODE_GENERIC, 4, 2, 256, ctypes.byref(m), fake, fake, fake, 1.0, fake,
+                               None, None) == swa.EINVAL
+        assert lib.swa_prefill_backward(4, 2, 256, ctypes.byref(m), fake, fake, fake, fake, fake, fake, 1.0, fake,
+                                        fake, fake, fake, 1 << 40, None) == swa.EINVAL
+    # a non-finite scale
+    m = swa.PrefillMeta(1, 100, 0, 100, 16, 0, None, None, None, plan)
+    assert lib.swa_prefill_backward(4, 2, 256, ctypes.byref(m), fake, fake, fake, fake, fake, fake, float("nan"),
+                                    fake, fake, fake, fake, 1 << 40, None) == swa.EINVAL
+    assert "scale" in swa.last_error()
