@@ -71,8 +71,8 @@ enum { SWA_MODE_CAUSAL = 0, SWA_MODE_GENERIC = 1 };
 enum { SWA_MASK_DECODE = 0, SWA_MASK_PREFILL = 1, SWA_MASK_DENSE_DEBUG = 2 };
 
 /* Rows added to the window by the compact buffer, and the roll period in
- * decode tokens ("window + 64 anchored buffers", "roll ... every 64 decode
- * tokens": [SPYRE] Summary). */
+ * decode tokens ([SPYRE] Summary: the compact buffer is W + 64 rows and rolls
+ * every 64 decode tokens). */
 #define SWA_ROLL_ROWS 64
 
 /* ------------------------------------------------------------------------ */
@@ -123,11 +123,14 @@ typedef struct swa_device_state {
 typedef struct swa_cache swa_cache; /* opaque host handle */
 
 /* Bytes of device memory a cache of this shape needs (state + valid_start +
- * K + V, each part 256-byte aligned).  Returns 0 for an invalid desc. */
+ * K + V, each part 256-byte aligned): the prompt-sized prefill cache and the
+ * W + 64-row compact buffer of [SPYRE] Summary, or the W-row ring of [BONSAI].
+ * Returns 0 for an invalid desc. */
 SWA_API size_t swa_cache_bytes(const swa_cache_desc* desc);
 
 /* Bind a cache to caller-owned device memory `dev_mem` (>= swa_cache_bytes,
- * 256-byte aligned), zero-fill it and write the initial state:
+ * 256-byte aligned), zero-fill it and write the initial state ([SPYRE]
+ * Summary and Compilation behavior: the index map lives in device data):
  *   prefill cache: origin 0, next_row S;   compact cache: origin S - W,
  *   next_row W (right-aligned anchoring; rows of negative positions stay
  *   zero and are never admitted by the mask);   ring: origin 0 (unused),
@@ -139,26 +142,31 @@ SWA_API swa_status swa_cache_alloc(const swa_cache_desc* desc, void* dev_mem, si
                                    const int32_t* dev_valid_start, swa_stream_t stream,
                                    swa_cache** out);
 
-/* Release the host handle only.  NULL is ignored. */
+/* Release the host handle only.  NULL is ignored.  (Library plumbing: the
+ * pages have no counterpart.) */
 SWA_API void swa_cache_free(swa_cache* cache);
 
 /* Resolved shape and device pointers of a cache (any out pointer may be NULL):
  * K and V base pointers ([layers, batch, kv_heads, rows, head_dim] bf16) and
- * the swa_device_state. */
+ * the swa_device_state.  (Library plumbing: the pages have no counterpart.) */
 SWA_API swa_status swa_cache_info(const swa_cache* cache, swa_cache_desc* desc_out, void** k_out,
                                   void** v_out, void** state_out);
 
-/* Host mirror of the index map: origin, next_row and decode steps taken. */
+/* Host mirror of the index map: origin, next_row and decode steps taken
+ * (the compact index of [SPYRE] Summary, kept on the host only to report
+ * misuse synchronously). */
 SWA_API swa_status swa_cache_position(const swa_cache* cache, int32_t* origin, int32_t* next_row,
                                       int32_t* step);
 
 /* Advance the host mirror by `steps` decode steps whose masks were built by
- * replaying a captured CUDA graph (a replay advances only the device state).
- * SWA_ESTATE if that would run past a due roll.  No CUDA call. */
+ * replaying a captured CUDA graph (a replay advances only the device state;
+ * one graph per fixed shape serves every position, [SPYRE] Compilation
+ * behavior).  SWA_ESTATE if that would run past a due roll.  No CUDA call. */
 SWA_API swa_status swa_cache_advance(swa_cache* cache, int32_t steps);
 
 /* Synchronise `stream` and report a device-side error recorded in the cache
- * state (SWA_EDEVICE), clearing it. */
+ * state (SWA_EDEVICE), clearing it.  (Library plumbing: the pages have no
+ * counterpart.) */
 SWA_API swa_status swa_cache_check(swa_cache* cache, swa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -194,7 +202,8 @@ typedef struct swa_prefill_meta {
   const void* plan;
 } swa_prefill_meta;
 
-/* Bytes of the device buffer swa_build_mask(SWA_MASK_PREFILL) fills. */
+/* Bytes of the device buffer swa_build_mask(SWA_MASK_PREFILL) fills (the
+ * generic prefill plan of [SPYRE] Compilation behavior). */
 SWA_API size_t swa_prefill_plan_bytes(const swa_prefill_meta* meta);
 
 /* Build a runtime mask on the device.
@@ -222,7 +231,9 @@ SWA_API swa_status swa_build_mask(swa_cache* cache, int32_t kind, const swa_pref
                                   void* dev_out, swa_stream_t stream);
 
 /* Report a device-side error recorded while building `plan` (SWA_EDEVICE,
- * e.g. an image block crossing the chunk end); synchronises `stream`. */
+ * e.g. an image block crossing the chunk end, or recorded by the backward
+ * pass that used it); synchronises `stream`.  ([SPYRE] Compilation behavior:
+ * the generic plan; the error word is this library's own.) */
 SWA_API swa_status swa_plan_check(const void* plan, swa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -257,7 +268,8 @@ SWA_API swa_status swa_prefill(swa_cache* cache, int32_t layer, int32_t mode, in
  * swa_last_error set on invalid arguments.  The score tiles dominate it:
  * 3 x 32 KB per (sequence, query head, 128-row query tile, key tile of its
  * band), the band being 1 + ceil((W - 1) / 128) key tiles without images and
- * every key tile with them. */
+ * every key tile with them.  (The training pass of "Add SDPA attention
+ * implementation", Summary; the workspace layout is this library's own.) */
 SWA_API size_t swa_prefill_backward_workspace_bytes(int32_t q_heads, const swa_prefill_meta* meta);
 
 /* Gradients of swa_prefill's output with respect to q, k and v, for training
@@ -299,7 +311,9 @@ SWA_API swa_status swa_compact(const swa_cache* prefill, swa_cache* compact, swa
 /* Decode                                                                    */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace bytes swa_decode needs for this cache and query-head count. */
+/* Workspace bytes swa_decode needs for this cache and query-head count (the
+ * split-K scratch of the decode of [SPYRE] Summary; the split is this
+ * library's own). */
 SWA_API size_t swa_decode_workspace_bytes(const swa_cache* cache, int32_t q_heads);
 
 /* One decode token of one sliding layer, after swa_build_mask(DECODE) of the
@@ -366,13 +380,14 @@ SWA_API swa_status swa_roll(swa_cache* cache, swa_stream_t stream);
 /* Diagnostics                                                               */
 /* ------------------------------------------------------------------------ */
 
-/* Message of the last failed call on this host thread ("" if none). */
+/* Message of the last failed call on this host thread ("" if none).
+ * (Library plumbing: the pages have no counterpart.) */
 SWA_API const char* swa_last_error(void);
 
-/* Static name of a status code. */
+/* Static name of a status code.  (Library plumbing.) */
 SWA_API const char* swa_status_string(swa_status status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  (Library plumbing.) */
 SWA_API int32_t swa_version(void);
 
 #ifdef __cplusplus

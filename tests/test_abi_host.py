@@ -170,3 +170,17 @@ def test_degenerate_sizes_are_rejected_on_the_host(swa):
     assert lib.swa_prefill_backward(4, 2, 256, ctypes.byref(m), fake, fake, fake, fake, fake, fake, float("nan"),
                                     fake, fake, fake, fake, 1 << 40, None) == swa.EINVAL
     assert "scale" in swa.last_error()
+
+
+def test_every_declaration_cites_its_source():
+    """Each entry point's comment names the page passage that defines it, or
+    says that it is library plumbing with no counterpart in the pages."""
+    text = open(HEADER).read()
+    blocks = re.findall(r"(/\*(?:[^*]|\*(?!/))*\*/)\s*\n(SWA_API[^;]*;)", text)
+    names = set()
+    for comment, decl in blocks:
+        name = re.search(r"\b(swa_\w+)\s*\(", decl).group(1)
+        names.add(name)
+        assert re.search(r"\[SPYRE\]|\[FASTLLM\]|\[BONSAI\]|Add SDPA attention|no counterpart|Library plumbing",
+                         comment), name
+    assert names == set(declared_functions())
