@@ -151,10 +151,13 @@ struct PrefillArgs {
   int32_t* err;                // device error word (cache state or plan header)
 };
 
-// Tensor-core (tcgen05) prefill: head size 256 in one CTA on 128-key tiles
-// (launch_prefill_t128), 512 in CTA pairs on 64-key tiles.
+// Tensor-core (tcgen05) prefill.  Head size 256: the two query heads of a
+// KV head share a CTA pair on 128-key tiles when the group size is even
+// (launch_prefill_pair256), else one CTA per head on 128-key tiles
+// (launch_prefill_t128).  Head size 512: CTA pairs on 64-key tiles.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_t128(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s);
 
 // 4-D bf16 tensor map with a {64, box_rows, 1, 1} box and 128-byte swizzle
 // (dims innermost first, strides in bytes of dims 1..3); false on failure.

@@ -1,5 +1,6 @@
 // Prefill attention on the 5th-generation tensor cores (tcgen05) on 64-key
-// tiles, for head size 512 (head size 256 runs prefill128_kernel).
+// tiles, for head size 512 (head size 256 runs prefill_pair256_kernel or
+// prefill128_kernel).
 //
 // One CTA computes 128 query rows of one query head, over a 256-column slice
 // of the head dimension, against the key tiles (64 keys each) its rows need;
@@ -825,7 +826,8 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4], co
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
-  if (a.head_dim == 256) return launch_prefill_t128(a, s);
+  if (a.head_dim == 256)
+    return (a.q_heads / a.kv_heads) % 2 == 0 ? launch_prefill_pair256(a, s) : launch_prefill_t128(a, s);
   const uint64_t D = uint64_t(a.head_dim);
   CUtensorMap mq, mk, mv;
   // query heads 2g and 2g + 1 share a KV head when the group size is even:
