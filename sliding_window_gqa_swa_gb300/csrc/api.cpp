@@ -418,11 +418,6 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
       return fail(SWA_EINVAL, "meta (seq_len, window) does not match the cache");
     if (meta->cu_seqlens) return fail(SWA_EINVAL, "packed documents take no cache");
     if ((k == nullptr) != (v == nullptr)) return fail(SWA_EINVAL, "k and v must both be given or both NULL");
-    if (k) {
-      cudaError_t e = swa::launch_write_rows(c->k, c->v, k, v, d.batch, meta->chunk_len, d.kv_heads,
-                                             d.head_dim, d.rows, layer, meta->chunk_start, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "write_rows launch");
-    }
     const long long slab = (long long)d.rows * d.head_dim;
     a.k = c->k + (long long)layer * d.batch * d.kv_heads * slab;
     a.v = c->v + (long long)layer * d.batch * d.kv_heads * slab;
@@ -432,6 +427,29 @@ swa_status swa_prefill(swa_cache* c, int32_t layer, int32_t mode, int32_t q_head
     a.key_rows = meta->chunk_start + meta->chunk_len;
     a.key_dim_rows = d.rows;
     a.err = &c->state->error;
+    if (k) {
+      // the chunk's K/V go into the cache rows [chunk_start, chunk_start + C):
+      // either before the attention kernel (which then reads every key from
+      // the cache), or concurrently with it when it reads the chunk's keys
+      // from k / v
+      a.k_in = reinterpret_cast<const uint16_t*>(k);
+      a.v_in = reinterpret_cast<const uint16_t*>(v);
+      const bool concurrent = swa::prefill_reads_chunk_inputs(a);
+      if (!concurrent) {
+        a.k_in = a.v_in = nullptr;
+        cudaError_t e = swa::launch_write_rows(c->k, c->v, k, v, d.batch, meta->chunk_len, d.kv_heads, d.head_dim,
+                                               d.rows, layer, meta->chunk_start, false, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "write_rows launch");
+      }
+      cudaError_t e = swa::launch_prefill_tc(a, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+      if (concurrent) {
+        e = swa::launch_write_rows(c->k, c->v, k, v, d.batch, meta->chunk_len, d.kv_heads, d.head_dim, d.rows,
+                                   layer, meta->chunk_start, true, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "write_rows launch");
+      }
+      return SWA_OK;
+    }
   } else {
     if (!meta->cu_seqlens) return fail(SWA_EINVAL, "without a cache, prefill needs packed documents (cu_seqlens)");
     if (mode != SWA_MODE_GENERIC) return fail(SWA_EINVAL, "packed documents use SWA_MODE_GENERIC");

@@ -20,10 +20,15 @@ __global__ void init_state_kernel(swa_device_state* st, int32_t* vs_dst, const i
 }
 
 // Chunk K/V [B, C, Hkv, D] -> cache rows [c0, c0 + C) of one layer.
+// kAfterReader: a programmatic dependent launch behind a prefill kernel that
+// reads the chunk's keys from k / v (not from these cache rows): the copy
+// starts at once and waits for that kernel only before exiting.
+template <bool kAfterReader>
 __global__ void write_rows_kernel(uint4* __restrict__ ck, uint4* __restrict__ cv,
                                   const uint4* __restrict__ k, const uint4* __restrict__ v,
                                   int batch, int chunk_len, int kv_heads, int d8, int rows,
                                   int layer, int c0) {
+  if (kAfterReader && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long n = (long long)batch * chunk_len * kv_heads * d8;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
@@ -38,6 +43,7 @@ __global__ void write_rows_kernel(uint4* __restrict__ ck, uint4* __restrict__ cv
     ck[dst] = k[i];
     cv[dst] = v[i];
   }
+  if (kAfterReader) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Compact rows [0, W) <- prefill rows [S - W, S) (zero for negative positions).
@@ -123,15 +129,31 @@ cudaError_t launch_init_state(swa_device_state* st, int32_t* vs_dst, const int32
 
 cudaError_t launch_write_rows(uint16_t* cache_k, uint16_t* cache_v, const uint16_t* k,
                               const uint16_t* v, int batch, int chunk_len, int kv_heads,
-                              int head_dim, int rows, int layer, int chunk_start, cudaStream_t s) {
+                              int head_dim, int rows, int layer, int chunk_start, bool after_reader,
+                              cudaStream_t s) {
   const int d8 = head_dim / 8;
   const long long n = (long long)batch * chunk_len * kv_heads * d8;
   if (n == 0) return cudaSuccess;
-  write_rows_kernel<<<grid_for(n, 256), 256, 0, s>>>(
-      reinterpret_cast<uint4*>(cache_k), reinterpret_cast<uint4*>(cache_v),
-      reinterpret_cast<const uint4*>(k), reinterpret_cast<const uint4*>(v), batch, chunk_len,
-      kv_heads, d8, rows, layer, chunk_start);
-  return cudaGetLastError();
+  uint4* ck = reinterpret_cast<uint4*>(cache_k);
+  uint4* cv = reinterpret_cast<uint4*>(cache_v);
+  const uint4* k4 = reinterpret_cast<const uint4*>(k);
+  const uint4* v4 = reinterpret_cast<const uint4*>(v);
+  if (!after_reader) {
+    write_rows_kernel<false><<<grid_for(n, 256), 256, 0, s>>>(ck, cv, k4, v4, batch, chunk_len, kv_heads, d8, rows,
+                                                              layer, chunk_start);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(n, 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, write_rows_kernel<true>, ck, cv, k4, v4, batch, chunk_len, kv_heads, d8, rows,
+                            layer, chunk_start);
 }
 
 cudaError_t launch_compact(uint16_t* dk, uint16_t* dv, const uint16_t* sk, const uint16_t* sv,

@@ -76,9 +76,14 @@ __host__ __device__ inline void causal_interval(int q, int vs, int window, int& 
 cudaError_t launch_init_state(swa_device_state* st, int32_t* vs_dst, const int32_t* vs_src,
                               int batch, swa_device_state init, cudaStream_t s);
 
+// after_reader: launched right after a prefill kernel that reads the chunk's
+// keys from its inputs, as a programmatic dependent launch: the copy may run
+// on SMs that kernel leaves idle, and the kernel does not complete before the
+// prefill kernel has (so later work on the stream stays ordered after both).
 cudaError_t launch_write_rows(uint16_t* cache_k, uint16_t* cache_v, const uint16_t* k,
                               const uint16_t* v, int batch, int chunk_len, int kv_heads,
-                              int head_dim, int rows, int layer, int chunk_start, cudaStream_t s);
+                              int head_dim, int rows, int layer, int chunk_start, bool after_reader,
+                              cudaStream_t s);
 
 // ring: position pos goes to row pos % window instead of row pos - (S - W)
 cudaError_t launch_compact(uint16_t* dk, uint16_t* dv, const uint16_t* sk, const uint16_t* sv,
@@ -149,6 +154,11 @@ struct PrefillArgs {
   int generic;
   float scale_log2;
   int32_t* err;                // device error word (cache state or plan header)
+  // The chunk's own K/V [B, C, Hkv, D] when the kernel reads keys
+  // [chunk_start, chunk_start + C) from them instead of the cache (which the
+  // K/V write then fills concurrently); null: every key comes from k / v.
+  const uint16_t* k_in;
+  const uint16_t* v_in;
 };
 
 // Tensor-core (tcgen05) prefill.  Head size 256: the two query heads of a
@@ -158,6 +168,9 @@ struct PrefillArgs {
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_t128(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s);
+// True when launch_prefill_tc runs the pair kernel for these arguments and it
+// can read the chunk's keys from k_in / v_in (the chunk starts on a key tile).
+bool prefill_reads_chunk_inputs(const PrefillArgs& a);
 
 // 4-D bf16 tensor map with a {64, box_rows, 1, 1} box and 128-byte swizzle
 // (dims innermost first, strides in bytes of dims 1..3); false on failure.

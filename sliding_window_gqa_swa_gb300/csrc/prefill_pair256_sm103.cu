@@ -68,13 +68,18 @@ constexpr int QBOX = 128 * 128;  // one {64 columns, 128 rows} bf16 box: 16 KB
 constexpr int KBOX = 64 * 128;   // one {64 columns, 64 keys} bf16 box: 8 KB
 constexpr int SLOT = 32768;      // K half-tile (64 keys x 256) or V half-tile (128 keys x 128)
 constexpr int NST = 4;           // ring slots
-constexpr int THREADS = 320;
+constexpr int THREADS = 512;
+// Per-thread registers after the split (launch: 65536 / 512 = 128 each); the
+// four warpgroups' shares add up to the launch's 65536 registers
+constexpr int REGS_CTRL = 56, REGS_SOFTMAX = 168, REGS_EPI = 120;
+static_assert(REGS_CTRL + 2 * REGS_SOFTMAX + REGS_EPI <= 4 * (65536 / THREADS), "register split");
 constexpr int OFF_Q = 0;
 constexpr int OFF_RING = OFF_Q + 4 * QBOX;
 constexpr int OFF_STAGE = OFF_RING + NST * SLOT;  // output staging: two {64 columns, 128 rows} boxes
-constexpr int OFF_PMAX = OFF_STAGE + 2 * QBOX;    // [2 groups][128 rows] fp32
-constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
-constexpr int N_BARS = 2 * NST + 10;
+constexpr int OFF_PMAX = OFF_STAGE + 2 * QBOX;    // [128 rows] fp32: the two groups' exchange
+constexpr int OFF_ROWS = OFF_PMAX + BM * 4;       // [128 rows] x {1 / l, lse}: softmax -> epilogue
+constexpr int OFF_BAR = OFF_ROWS + BM * 8;
+constexpr int N_BARS = 2 * NST + 11;
 constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
 constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack to align the base to 1024 B
 static_assert(SMEM <= 232448, "shared memory budget");
@@ -100,6 +105,7 @@ struct Bars {
   __device__ uint32_t teardown() const { return base + 8 * (2 * NST + 7); }
   __device__ uint32_t q_free() const { return base + 8 * (2 * NST + 8); }  // the item's score MMAs are done
   __device__ uint32_t o_free() const { return base + 8 * (2 * NST + 9); }  // the epilogue has read O
+  __device__ uint32_t rows_ready() const { return base + 8 * (2 * NST + 10); }  // 1 / l and lse of every row
 };
 
 // Bounded wait on one phase of an mbarrier (cluster-scope acquire when the
@@ -123,13 +129,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-// Bounded wait for a phase that another CTA's arrivals complete: polled with
-// test_wait (a suspended try_wait is not always woken promptly by a remote arrive).
-__device__ __forceinline__ bool wait_poll(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
+// Bounded wait of a single thread on the critical path (the MMA issuer and
+// the forwarder): polled with test_wait, because a thread suspended in
+// try_wait was measured to resume up to ~1500 SM clocks after the phase
+// completed.  kCluster: acquire at cluster scope (the peer's arrivals).
+template <bool kCluster>
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  auto poll = [&] {
+    if (!kCluster) return mbar_test_wait(bar, parity);
+    if (!mbar_test_wait_relaxed_cluster(bar, parity)) return false;
+    fence_acquire_cluster();
+    return true;
+  };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (poll()) return true;
     if ((it & 255) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kTimeoutNs) {
@@ -179,13 +194,6 @@ __device__ __forceinline__ float pair_sum(uint64_t x) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
   return lo + hi;
-}
-
-// 32-byte store of 8 words (the address is 32-byte aligned)
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
 }
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
@@ -238,6 +246,7 @@ __device__ __forceinline__ void tile_range(const PrefillArgs& a, int b, int qt, 
 __global__ void __launch_bounds__(THREADS, 1)
 prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       const __grid_constant__ CUtensorMap tm_ki, const __grid_constant__ CUtensorMap tm_vi,
                        const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -271,7 +280,8 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       mbar_init(bars.p_full(i), issuer ? 257 : 256);
       mbar_init(bars.pv_done(i), 1);
     }
-    mbar_init(bars.o_free(), issuer ? 257 : 256);
+    mbar_init(bars.o_free(), issuer ? 129 : 128);
+    mbar_init(bars.rows_ready(), 128);
     mbar_init(bars.teardown(), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -285,12 +295,24 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_o);
+    if (a.k_in) {
+      prefetch_tmap(&tm_ki);
+      prefetch_tmap(&tm_vi);
+    }
   }
   tc_fence_before();
   cluster_sync();  // the peer's barriers are initialised before any remote arrive or copy
   tc_fence_after();
+  // programmatic dependent launch: the K/V write launched behind this kernel
+  // may start now (it reads only the chunk's inputs); this kernel's own inputs
+  // are read after the wait for the kernel launched before it
+  if (threadIdx.x == 0) pdl_launch_dependents();
+  pdl_wait();
   const uint32_t tmem = *tmem_slot;
 
+  // each role's code follows its warpgroup's register split in the same branch
+  if (warp < 4) {
+  regs_dec<REGS_CTRL>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Per item: Q (once the previous item's score products are done), then the
@@ -302,16 +324,21 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       const int s = idx % NST;
       ok = __all_sync(0xffffffffu, wait_bar<false>(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
       if (ok && lane == 0) {
-        const int k0 = kt * BN;
+        int k0 = kt * BN;
         const uint32_t dst = sRing + s * SLOT;
         const uint32_t bar = map_shared(bars.full(s), 0);
         if (issuer) mbar_arrive_expect_tx(bars.full(s), 2 * SLOT);
+        // keys of the chunk itself come from its inputs when the kernel reads them
+        const bool from_in = a.k_in != nullptr && k0 >= a.chunk_start;
+        if (from_in) k0 -= a.chunk_start;
         if (is_v) {
           // head-dimension columns [128 crank, 128 crank + 128) of all 128 keys
-          for (int c = 0; c < 2; ++c) tma_load_4d_pair(dst + c * QBOX, &tm_v, bar, 128 * crank + 64 * c, k0, hk, b);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d_pair(dst + c * QBOX, from_in ? &tm_vi : &tm_v, bar, 128 * crank + 64 * c, k0, hk, b);
         } else {
           // keys [k0 + 64 crank, k0 + 64 crank + 64), all 256 columns
-          for (int c = 0; c < 4; ++c) tma_load_4d_pair(dst + c * KBOX, &tm_k, bar, 64 * c, k0 + 64 * crank, hk, b);
+          for (int c = 0; c < 4; ++c)
+            tma_load_4d_pair(dst + c * KBOX, from_in ? &tm_ki : &tm_k, bar, 64 * c, k0 + 64 * crank, hk, b);
         }
       }
       __syncwarp();
@@ -360,10 +387,10 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         int kt_lo, n;
         tile_range(a, x.b, x.qt, kt_lo, n);
         if (n == 0) continue;
-        ok = wait_bar<false>(bars.q(), qn & 1, abort_flag, err);
+        ok = wait_spin<false>(bars.q(), qn & 1, abort_flag, err);
         ++qn;
         for (int t = 0; t < 2 && t < n && ok; ++t) {
-          ok = wait_bar<false>(bars.full(idx % NST), (idx / NST) & 1, abort_flag, err);
+          ok = wait_spin<false>(bars.full(idx % NST), (idx / NST) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           qk((T + t) & 1, idx % NST);
@@ -375,19 +402,19 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         // V_j and K_{j+2} of tile j landed: tile 0 here, tile j + 1 right after
         // tile j's MMAs are issued (the wait overlaps their execution)
         auto wait_data = [&](int j) {
-          return wait_bar<false>(bars.full(idx % NST), (idx / NST) & 1, abort_flag, err) &&
-                 (j + 2 >= n || wait_bar<false>(bars.full((idx + 1) % NST), ((idx + 1) / NST) & 1, abort_flag, err));
+          return wait_spin<false>(bars.full(idx % NST), (idx / NST) & 1, abort_flag, err) &&
+                 (j + 2 >= n || wait_spin<false>(bars.full((idx + 1) % NST), ((idx + 1) / NST) & 1, abort_flag, err));
         };
         if (ok) ok = wait_data(0);
         // the previous item's epilogue has read O (both CTAs) before PV_0 overwrites it
-        if (ok && on > 0) ok = wait_poll(bars.o_free(), (on - 1) & 1, abort_flag, err);
+        if (ok && on > 0) ok = wait_spin<true>(bars.o_free(), (on - 1) & 1, abort_flag, err);
         ++on;
         for (int j = 0; j < n && ok; ++j) {
           const int tj = T + j, sb = tj & 1;
           const bool next = j + 2 < n;  // S_{j+2} goes to the buffer S_j came from
           const int sv = idx % NST, sk = (idx + 1) % NST;
           // P_j written in both CTAs (its data landed already)
-          ok = wait_poll(bars.p_full(sb), (tj >> 1) & 1, abort_flag, err);
+          ok = wait_spin<true>(bars.p_full(sb), (tj >> 1) & 1, abort_flag, err);
           if (!ok) break;
           tc_fence_after();
           const uint32_t vslot = sRing + sv * SLOT;
@@ -412,7 +439,7 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
         T += n;
       }
-    } else if (!issuer) {
+    } else if (!issuer && lane == 0) {
       // ---------------------------------------------------------- forwarder
       // each P_j and each finished epilogue of this CTA is announced to the
       // issuing CTA with one cluster-scope arrival
@@ -425,29 +452,40 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (n == 0) continue;
         for (int j = 0; j < n && ok; ++j) {
           const int tj = T + j;
-          ok = __all_sync(0xffffffffu, wait_bar<false>(bars.p_full(tj & 1), (tj >> 1) & 1, abort_flag, err));
-          if (ok && lane == 0) mbar_arrive_remote(map_shared(bars.p_full(tj & 1), 0));
-          __syncwarp();
+          ok = wait_spin<false>(bars.p_full(tj & 1), (tj >> 1) & 1, abort_flag, err);
+          // the softmax threads' tcgen05.wait::st preceded their local arrivals
+          if (ok) mbar_arrive_remote_relaxed(map_shared(bars.p_full(tj & 1), 0));
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar<false>(bars.o_free(), on & 1, abort_flag, err));
-        if (ok && lane == 0) mbar_arrive_remote(map_shared(bars.o_free(), 0));
-        __syncwarp();
+        if (ok) ok = wait_spin<false>(bars.o_free(), on & 1, abort_flag, err);
+        if (ok) mbar_arrive_remote_relaxed(map_shared(bars.o_free(), 0));
         ++on;
         T += n;
       }
     }
-  } else {
+  }
+  } else if (warp < 12) {
+    regs_inc<REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax
-    const int grp = (warp - 2) >> 2;
+    const int grp = (warp - 4) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     constexpr int HC = BN / 2;  // key columns per group
-    constexpr int OC = HD / 2;  // output columns per group
     const int cb = grp * HC;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    float* pmax = reinterpret_cast<float*>(gbase + OFF_PMAX);  // [group][row]
+    // the two groups of a row exchange through one value per row: group 0
+    // writes, both meet, group 1 combines and writes, both meet, group 0 reads
+    float* xch = reinterpret_cast<float*>(gbase + OFF_PMAX) + r;
+    float2* rows = reinterpret_cast<float2*>(gbase + OFF_ROWS) + r;
     const int bar_id = 1 + q4;  // named barrier of this quadrant's two warps
     const float c2 = a.scale_log2;
+    auto combine = [&](float v, bool is_max) {
+      if (grp == 0) *xch = v;
+      named_sync(bar_id);
+      if (grp == 1) *xch = v = is_max ? fmaxf(v, *xch) : v + *xch;
+      named_sync(bar_id);
+      if (grp == 0) v = *xch;
+      return v;
+    };
     // The two warps of a row meet at a named barrier for every tile and at the
     // end of every item; a warp that gives up (timeout or abort) keeps meeting
     // its partner there and skips the rest, so the arrivals stay paired.
@@ -455,13 +493,13 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     int T = 0;
     for (int it = cid; it < nitems; it += ncl) {
       const Item x = item_of(it, npairs, a.batch, nqt);
-      const int hq = 2 * x.pair + crank, b = x.b;
+      const int b = x.b;
       int kt_lo, n;
       tile_range(a, b, x.qt, kt_lo, n);
+      if (n == 0) continue;  // the epilogue warps write the zero rows
       const int i = x.qt * BM + r;
-      const bool row_ok = i < a.chunk_len;
       int lo = 0, hi = -1;
-      if (row_ok && n > 0) {
+      if (i < a.chunk_len) {
         if (a.generic) {
           const PlanLayout L = plan_layout(a.batch, a.chunk_len);
           const char* plan = static_cast<const char*>(a.plan);
@@ -482,21 +520,27 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         if (ok) ok = __all_sync(0xffffffffu, wait_bar<true>(bars.s_full(sb), (tt >> 1) & 1, abort_flag, err));
         if (ok) tc_fence_after();
         const uint32_t tS = tmem + lane_off + TM_S + sb * BN;
-        const int k0 = (kt_lo + t) * BN;
-        const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
+        // this group's keys [k0, k0 + 64): columns outside the row's interval are masked
+        const int k0 = (kt_lo + t) * BN + cb;
+        const bool need_lo = !__all_sync(0xffffffffu, k0 >= lo);
+        const bool need_hi = !__all_sync(0xffffffffu, k0 + HC - 1 <= hi);
         uint32_t sr[HC];
         float mraw = -CUDART_INF_F;
         if (ok) {
           tmem_ld32(tS + cb, sr);
           tmem_ld32(tS + cb + 32, sr + 32);
           tmem_ld_wait();
-          if (masked) {
-            // column c is admitted iff clo <= c <= chi (an empty interval admits none)
-            const int clo = lo - (k0 + cb);
-            const uint32_t span = uint32_t(hi - lo);
+          const int clo = lo - k0, chi = hi - k0;  // admitted columns [clo, chi]
+          if (need_lo && need_hi) {
 #pragma unroll
             for (int c = 0; c < HC; ++c)
-              sr[c] = (uint32_t(c - clo) <= span && hi >= lo) ? sr[c] : __float_as_uint(-CUDART_INF_F);
+              sr[c] = (c >= clo && c <= chi) ? sr[c] : __float_as_uint(-CUDART_INF_F);
+          } else if (need_hi) {  // the diagonal tile: a prefix of the columns
+#pragma unroll
+            for (int c = 0; c < HC; ++c) sr[c] = c <= chi ? sr[c] : __float_as_uint(-CUDART_INF_F);
+          } else if (need_lo) {  // the tile at the window's start: a suffix
+#pragma unroll
+            for (int c = 0; c < HC; ++c) sr[c] = c >= clo ? sr[c] : __float_as_uint(-CUDART_INF_F);
           }
           float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
@@ -509,11 +553,8 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           mraw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
         // the two groups of this row agree on the tile maximum; after this
-        // barrier both have read their S columns, so P may overwrite them
-        pmax[grp * BM + r] = mraw;
-        named_sync(bar_id);
-        mraw = fmaxf(mraw, pmax[(grp ^ 1) * BM + r]);
-        named_sync(bar_id);
+        // exchange both have read their S columns, so P may overwrite them
+        mraw = combine(mraw, true);
         if (!ok) continue;
         const float mt = mraw * c2;
         // lazy rescale: move the reference only when the maximum grows by > 2^32
@@ -526,7 +567,7 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
           tc_fence_after();
           const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
 #pragma unroll 1
-          for (int c0 = grp * OC; c0 < grp * OC + OC; c0 += 16) {
+          for (int c0 = grp * (HD / 2); c0 < (grp + 1) * (HD / 2); c0 += 16) {
             uint32_t o[16];
             tmem_ld16(tmem + lane_off + TM_O + c0, o);
             tmem_ld_wait();
@@ -564,70 +605,116 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         tc_fence_before();
         mbar_arrive(bars.p_full(sb));
       }
-      // row sums of both groups
-      pmax[grp * BM + r] = l_run;
-      named_sync(bar_id);
-      const float l_tot = l_run + pmax[(grp ^ 1) * BM + r];
-      named_sync(bar_id);
-      pmax[grp * BM + r] = l_exact;
-      named_sync(bar_id);
-      const float e_tot = l_exact + pmax[(grp ^ 1) * BM + r];
-      named_sync(bar_id);  // both have read before the next item reuses the exchange
-      // epilogue: O / l -> bf16, this group's output columns
-      bool have_o = n > 0 && ok;
-      if (have_o)
-        have_o = __all_sync(0xffffffffu, wait_bar<true>(bars.pv_done((T + n - 1) & 1), ((T + n - 1) >> 1) & 1,
-                                                        abort_flag, err));
-      tc_fence_after();
-      const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-      // this group's 128 output columns as 64 bf16 pairs; O is released as soon
-      // as it is read, before the stores
-      uint32_t ow[OC / 2];
+      // the row's normaliser and lse go to the epilogue warps (group 0 holds both
+      // groups' sums after the exchanges); their previous values were read
+      // before the epilogue released O for this item's first PV
+      const float l_tot = combine(l_run, false);
+      const float e_tot = combine(l_exact, false);
+      if (grp == 0) {
+        *rows = make_float2(l_tot > 0.f ? 1.f / l_tot : 0.f,
+                            e_tot > 0.f ? (m_run + log2f(e_tot)) * 0.69314718055994530942f : -CUDART_INF_F);
+        mbar_arrive(bars.rows_ready());
+      }
+      T += n;
+    }
+  } else {
+    regs_dec<REGS_EPI>();
+    // ------------------------------------------------------------ epilogue
+    // Per item: O (this thread's row, 256 columns) / l -> bf16 -> the staging
+    // boxes -> TMA stores, in two rounds of 128 columns; O is released for the
+    // next item's first PV as soon as the second round's columns are read
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    const float2* rows = reinterpret_cast<const float2*>(gbase + OFF_ROWS) + r;
+    const bool elected = warp == 12 && lane == 0;
+    uint8_t* stage_row = gbase + OFF_STAGE + r * 128;
+    auto epi_sync = [] { asm volatile("bar.sync 5, 128;" ::: "memory"); };
+    // bf16 pair u (0..7) of 16-byte unit `unit` of this row in staging box g
+    auto put = [&](int g, int unit, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+      *reinterpret_cast<uint4*>(stage_row + g * QBOX + ((unit ^ (r & 7)) << 4)) = make_uint4(x0, x1, x2, x3);
+    };
+    // the staging boxes hold head-dimension columns [128 h, 128 h + 128): store them
+    auto flush = [&](int h, int qt, int hq, int b) {
+      fence_proxy_async_smem();
+      epi_sync();
+      if (elected) {
+        for (int g = 0; g < 2; ++g) tma_store_4d(&tm_o, base + OFF_STAGE + g * QBOX, 128 * h + 64 * g, qt * BM, hq, b);
+        bulk_commit_group();
+      }
+    };
+    auto staging_free = [&] {
+      if (elected) bulk_wait_read_all();  // the previous round's stores have read the staging
+      epi_sync();
+    };
+    bool ok = true;
+    int T = 0, on = 0;
+    for (int it = cid; it < nitems; it += ncl) {
+      const Item x = item_of(it, npairs, a.batch, nqt);
+      const int hq = 2 * x.pair + crank, b = x.b;
+      int kt_lo, n;
+      tile_range(a, b, x.qt, kt_lo, n);
+      const int i = x.qt * BM + r;
+      float inv = 0.f, lse = -CUDART_INF_F;
+      bool have_o = false;
+      if (n > 0) {
+        if (ok) ok = __all_sync(0xffffffffu, wait_bar<false>(bars.rows_ready(), on & 1, abort_flag, err));
+        if (ok)
+          ok = __all_sync(0xffffffffu, wait_bar<true>(bars.pv_done((T + n - 1) & 1), ((T + n - 1) >> 1) & 1,
+                                                      abort_flag, err));
+        tc_fence_after();
+        have_o = ok;
+        if (ok) {
+          const float2 v = *rows;
+          inv = v.x;
+          lse = v.y;
+        }
+      }
+      auto cvt = [&](const uint32_t* o, int e) {
+        return have_o ? pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv) : 0u;
+      };
+      // round 0: columns [0, 128) straight into the staging boxes
+      staging_free();
 #pragma unroll
-      for (int h = 0; h < OC / 16; ++h) {
-        uint32_t o[16];
+      for (int h4 = 0; h4 < 4; ++h4) {
+        uint32_t o[32];
         if (have_o) {
-          tmem_ld16(tmem + lane_off + TM_O + grp * OC + 16 * h, o);
+          tmem_ld32(tmem + lane_off + TM_O + 32 * h4, o);
           tmem_ld_wait();
         }
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          ow[8 * h + e] = have_o ? pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv) : 0u;
+        for (int u = 0; u < 4; ++u)
+          put(h4 >> 1, (h4 & 1) * 4 + u, cvt(o, 4 * u), cvt(o, 4 * u + 1), cvt(o, 4 * u + 2), cvt(o, 4 * u + 3));
+      }
+      flush(0, x.qt, hq, b);
+      // round 1: columns [128, 256) into registers; then O is free
+      uint32_t w[64];
+#pragma unroll
+      for (int h8 = 0; h8 < 8; ++h8) {
+        uint32_t o[16];
+        if (have_o) {
+          tmem_ld16(tmem + lane_off + TM_O + 128 + 16 * h8, o);
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[8 * h8 + e] = cvt(o, e);
       }
       if (n > 0) {  // O read: the next item's first PV may overwrite it
         tc_fence_before();
         mbar_arrive(bars.o_free());
+        ++on;
       }
-      // the output leaves in two rounds of 64 columns per group through the
-      // staging boxes (128-byte swizzled rows, as the tensor map reads them);
-      // rows past the chunk end are clipped by the store
-      const bool elected = warp == 2 && lane == 0;
-      uint8_t* box = gbase + OFF_STAGE + grp * QBOX + r * 128;
+      staging_free();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (elected) bulk_wait_read_all();  // the previous round's stores have read the staging
-        asm volatile("bar.sync 5, 256;" ::: "memory");
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(box + ((u ^ (r & 7)) << 4)) =
-              make_uint4(ow[32 * h + 4 * u], ow[32 * h + 4 * u + 1], ow[32 * h + 4 * u + 2], ow[32 * h + 4 * u + 3]);
-        fence_proxy_async_smem();
-        asm volatile("bar.sync 5, 256;" ::: "memory");
-        if (elected) {
-          for (int g = 0; g < 2; ++g)
-            tma_store_4d(&tm_o, base + OFF_STAGE + g * QBOX, g * OC + 64 * h, x.qt * BM, hq, b);
-          bulk_commit_group();
-        }
-      }
-      if (row_ok && a.lse && grp == 0)
-        a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] =
-            e_tot > 0.f ? (m_run + log2f(e_tot)) * 0.69314718055994530942f : -CUDART_INF_F;
+      for (int u = 0; u < 16; ++u) put(u >> 3, u & 7, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+      flush(1, x.qt, hq, b);
+      if (a.lse && i < a.chunk_len) a.lse[((long long)b * a.chunk_len + i) * a.q_heads + hq] = lse;
       T += n;
     }
   }
 
   // ------------------------------------------------------------ teardown
-  if (warp == 2 && lane == 0) bulk_wait_all();  // the output stores have completed
+  if (warp == 12 && lane == 0) bulk_wait_all();  // the output stores have completed
   tc_fence_before();
   __syncthreads();
   if (*abort_flag) {
@@ -706,6 +793,14 @@ cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s) {
   if (!make_tmap_bf16(&mk, a.k, kd, ks, BN / 2) || !make_tmap_bf16(&mv, a.v, kd, ks, BN) ||
       !make_tmap_bf16(&mq, a.q, qd, qs, BM) || !make_tmap_bf16(&mo, a.out, qd, qs, BM))
     return cudaErrorInvalidValue;
+  // the chunk's own K/V [B, C, Hkv, D]: dims {D, C, Hkv, B}
+  CUtensorMap mki = mk, mvi = mv;
+  if (a.k_in) {
+    const uint64_t id[4] = {D, uint64_t(a.chunk_len), uint64_t(a.kv_heads), uint64_t(a.batch)};
+    const uint64_t is[3] = {uint64_t(a.kv_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.kv_heads * D * 2};
+    if (!make_tmap_bf16(&mki, a.k_in, id, is, BN / 2) || !make_tmap_bf16(&mvi, a.v_in, id, is, BN))
+      return cudaErrorInvalidValue;
+  }
   const int nqt = (a.chunk_len + BM - 1) / BM;
   const long long nitems = (long long)nqt * (a.q_heads / 2) * a.batch;
   const int ncl = int(std::min<long long>(nitems, max_clusters()));
@@ -714,14 +809,22 @@ cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = 2;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: set-up overlaps the previous kernel's tail
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_pair256_kernel, mq, mk, mv, mo, a);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, prefill_pair256_kernel, mq, mk, mv, mo, mki, mvi, a);
+}
+
+bool prefill_reads_chunk_inputs(const PrefillArgs& a) {
+  return a.head_dim == HD && (a.q_heads / a.kv_heads) % 2 == 0 && a.k_in != nullptr && a.v_in != nullptr &&
+         a.chunk_start % BN == 0;
 }
 
 }  // namespace swa

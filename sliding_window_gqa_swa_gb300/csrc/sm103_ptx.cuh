@@ -175,10 +175,44 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
   return ok != 0;
 }
 
+// Arrive on an mbarrier of another CTA of the cluster without release
+// semantics (the caller has already made its data visible, e.g. by
+// tcgen05.wait::st before a CTA-scope handoff).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Non-blocking test of one phase without acquire semantics (pair it with
+// fence_acquire_cluster once it succeeds).
+__device__ __forceinline__ bool mbar_test_wait_relaxed_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.relaxed.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void fence_acquire_cluster() { asm volatile("fence.acquire.cluster;" ::: "memory"); }
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (the tensor core reads its operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ register split
+// Every warp of a warpgroup executes the same instruction: the warpgroup's
+// per-thread register budget moves down (releasing registers) or up
+// (waiting until enough are released).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ launch chaining
