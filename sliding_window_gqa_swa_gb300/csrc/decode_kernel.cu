@@ -846,6 +846,8 @@ cudaError_t decode_static_scratch(void** ptr) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  // the latency regime (16 compute warps: few slabs) goes to the tensor-core kernel
+  if (a.warps == 16 && decode_small_eligible(a)) return launch_decode_small(a, s);
   switch (a.head_dim) {
     case 64: return launch_d<64>(a, s);
     case 128: return launch_d<128>(a, s);

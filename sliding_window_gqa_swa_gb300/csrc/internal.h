@@ -132,6 +132,12 @@ int decode_max_cluster();
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// Latency-regime decode (few slabs, one cluster per slab, at most 128 rows per
+// CTA, Hq / Hkv <= 2, head size 128-512): warp-level tensor-core products and
+// no merge between warps.  launch_decode uses it whenever eligible.
+bool decode_small_eligible(const DecodeArgs& a);
+cudaError_t launch_decode_small(const DecodeArgs& a, cudaStream_t s);
+
 // Device address, on the current device, of the static scratch array that
 // swa_decode_noalloc uses (SWA_DECODE_STATIC_SCRATCH_BYTES); looked up once
 // per device.
