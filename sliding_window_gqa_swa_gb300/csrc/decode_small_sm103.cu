@@ -77,23 +77,33 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x on the special-function unit (subnormal results flush to 0; -inf -> 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Shared memory (dynamic): K [RP][D] | V [RP][D] (swizzled bf16, RP = rows
-// rounded up to 16) | scores [G][RP] fp32 | P [G][RP] bf16 | O [G][D] fp32 |
-// mask bytes [RP].  The merge area is static.
+// rounded up to 16) | per-block statistics [3][G][8] fp32 (maximum, rounded
+// and unrounded sums of each 16-row block) | P [G][RP] bf16 | O [G][D] fp32 |
+// the step's new K and V rows [2][D] bf16 | mask bytes [RP].  The merge area
+// is static.
 template <int D>
 struct SmallLayout {
   static constexpr int U = D / 8;  // 16-byte units per row
   __host__ __device__ static size_t kv(int rp) { return size_t(rp) * D * 2; }
   __host__ __device__ static size_t off_v(int rp) { return kv(rp); }
   __host__ __device__ static size_t off_s(int rp) { return 2 * kv(rp); }
-  __host__ __device__ static size_t off_p(int rp, int g) { return off_s(rp) + size_t(g) * rp * 4; }
+  __host__ __device__ static size_t off_p(int rp, int g) { return off_s(rp) + size_t(3 * 8) * g * 4; }
   __host__ __device__ static size_t off_o(int rp, int g) { return (off_p(rp, g) + size_t(g) * rp * 2 + 15) & ~size_t(15); }
-  __host__ __device__ static size_t off_m(int rp, int g) { return off_o(rp, g) + size_t(g) * D * 4; }
+  __host__ __device__ static size_t off_n(int rp, int g) { return off_o(rp, g) + size_t(g) * D * 4; }
+  __host__ __device__ static size_t off_m(int rp, int g) { return off_n(rp, g) + size_t(2) * D * 2; }
   __host__ __device__ static size_t total(int rp, int g) { return off_m(rp, g) + size_t(rp); }
 };
 
@@ -118,9 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
 
   uint8_t* sK = smem;
   uint8_t* sV = smem + LY::off_v(RP);
-  float* sS = reinterpret_cast<float*>(smem + LY::off_s(RP));          // [G][RP]
+  float* sB = reinterpret_cast<float*>(smem + LY::off_s(RP));          // [3][G][8] block statistics
   uint16_t* sP = reinterpret_cast<uint16_t*>(smem + LY::off_p(RP, G));  // [G][RP]
   float* sO = reinterpret_cast<float*>(smem + LY::off_o(RP, G));        // [G][D]
+  uint8_t* sN = smem + LY::off_n(RP, G);                                // new K row | new V row
   uint8_t* mask_s = smem + LY::off_m(RP, G);
   __shared__ __align__(16) float4 s_recv[32 + kNf];  // 16 CTAs x 2 header items + accumulator slices
   __shared__ __align__(8) uint64_t s_merge_bar;
@@ -171,6 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
       bq[kk][1] = gq < G ? qp[kk * 8 + 4 + (lane & 3)] : 0u;
     }
   }
+  // the step's new row, in the same round trip (only the owning CTA uses it)
+  if (append && tid < 2 * U) {
+    const int kv = tid >= U, u = kv ? tid - U : tid;
+    cp_async_16(smem_u32(sN) + tid * 16, (kv ? a.v_new : a.k_new) + ((long long)b * a.kv_heads + h) * D + u * 8);
+  }
   const bool state_ok = cur >= 0 && cur < R;
   const int cur_i = (append && state_ok) ? cur - r0 : -1;
   cp_async_wait_all();
@@ -179,11 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
   if (nsplit > 1) asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   if (cur_i >= 0 && cur_i < nrows) {
     // this CTA owns the step's row: it replaces the prefetched row and is appended
-    const uint4* kn = reinterpret_cast<const uint4*>(a.k_new + ((long long)b * a.kv_heads + h) * D);
-    const uint4* vn = reinterpret_cast<const uint4*>(a.v_new + ((long long)b * a.kv_heads + h) * D);
     for (int u = tid; u < 2 * U; u += kThreads) {
       const int kv = u >= U, uu = kv ? u - U : u;
-      const uint4 x = kv ? vn[uu] : kn[uu];
+      const uint4 x = reinterpret_cast<const uint4*>(sN)[u];
       *reinterpret_cast<uint4*>((kv ? sV : sK) + swz(cur_i, uu, U)) = x;
       reinterpret_cast<uint4*>((kv ? Vc : Kc) + (long long)cur * D)[uu] = x;
     }
@@ -191,9 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
   if (!state_ok && split == 0 && tid == 0) atomicCAS(&st->error, 0, kErrRowRange);
   __syncthreads();
 
-  // ---- scores: warp w takes 16-row blocks w, w + 8, ...
+  // ---- scores: warp w takes 16-row blocks w, w + 8, ...  A lane holds rows
+  // rb * 16 + l / 4 (+ 8) of heads 2 (l % 4) (+ 1): for G <= 2 the lanes
+  // with l % 4 == 0.  Each block's maximum goes to shared memory; after one
+  // barrier every warp turns its own block into probabilities.
   const float c2 = a.scale_log2;
-  for (int rb = warp; rb < RP / 16; rb += kWarps) {
+  float sc[2][4];  // scores of this warp's blocks (exp2 domain; -inf when masked)
+  const int nblk = RP / 16;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rb = warp + t * kWarps;
+    if (rb >= nblk) break;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const int ar = rb * 16 + (lane & 15);  // row this lane addresses for ldmatrix
 #pragma unroll
@@ -202,47 +224,78 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
       ldsm_x4(kbase + swz(ar, 2 * kk + (lane >> 4), U), af[0], af[1], af[2], af[3]);
       mma16816(acc[kk & 1], af, bq[kk][0], bq[kk][1]);
     }
-    // lane holds rows rb * 16 + l / 4 (+ 8), heads 2 (l % 4) (+ 1)
+    float bm[2] = {-CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int g = 2 * (lane & 3) + (e & 1);
       const int rr = rb * 16 + (lane >> 2) + ((e & 2) ? 8 : 0);
-      if (g < G) {
-        const bool in = rr < nrows && state_ok && mask_s[rr] != 0;
-        sS[g * RP + rr] = in ? (acc[0][e] + acc[1][e]) * c2 : -CUDART_INF_F;
-      }
+      const bool in = (lane & 3) == 0 && rr < nrows && state_ok && mask_s[rr] != 0;
+      sc[t][e] = in ? (acc[0][e] + acc[1][e]) * c2 : -CUDART_INF_F;
+      bm[e & 1] = fmaxf(bm[e & 1], sc[t][e]);
+    }
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], o));
+      bm[1] = fmaxf(bm[1], __shfl_xor_sync(0xffffffffu, bm[1], o));
+    }
+    if (lane == 0) {  // the lanes with l % 4 == 0 were reduced into lane 0
+#pragma unroll
+      for (int g = 0; g < G; ++g) sB[g * 8 + rb] = bm[g];
     }
   }
   __syncthreads();
 
-  // ---- softmax over the CTA's rows: warp g takes head g
-  if (warp < G) {
-    const int g = warp;
-    float m = -CUDART_INF_F;
-    for (int rr = lane; rr < RP; rr += 32) m = fmaxf(m, sS[g * RP + rr]);
+  // ---- probabilities of the warp's blocks against the CTA maximum M: P in
+  // bf16; the block's rounded and unrounded sums
+  float M[G];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float nm = (m == -CUDART_INF_F) ? 0.f : -m;
-    float lr = 0.f, le = 0.f;
-    for (int rr = lane; rr < RP; rr += 32) {
-      const float p = exp2f(sS[g * RP + rr] + nm);  // -inf -> 0
-      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-      sP[g * RP + rr] = *reinterpret_cast<const uint16_t*>(&pb);
-      lr += __bfloat162float(pb);
-      le += p;
+  for (int g = 0; g < G; ++g) {
+    M[g] = -CUDART_INF_F;
+    for (int k = 0; k < nblk; ++k) M[g] = fmaxf(M[g], sB[g * 8 + k]);
+  }
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rb = warp + t * kWarps;
+    if (rb >= nblk) break;
+    float lr[2] = {0.f, 0.f}, le[2] = {0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int g = e & 1;
+      if (g < G && (lane & 3) == 0) {
+        const int rr = rb * 16 + (lane >> 2) + ((e & 2) ? 8 : 0);
+        const float p = ex2(sc[t][e] - (M[g] == -CUDART_INF_F ? 0.f : M[g]));  // -inf -> 0
+        const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+        sP[g * RP + rr] = *reinterpret_cast<const uint16_t*>(&pb);
+        lr[g] += __bfloat162float(pb);
+        le[g] += p;
+      }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lr += __shfl_xor_sync(0xffffffffu, lr, o);
-      le += __shfl_xor_sync(0xffffffffu, le, o);
+    for (int o = 4; o < 32; o <<= 1) {
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        lr[g] += __shfl_xor_sync(0xffffffffu, lr[g], o);
+        le[g] += __shfl_xor_sync(0xffffffffu, le[g], o);
+      }
     }
     if (lane == 0) {
-      s_M[g] = m;
-      s_L[g] = lr;
-      s_E[g] = le;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        sB[(G + g) * 8 + rb] = lr[g];
+        sB[(2 * G + g) * 8 + rb] = le[g];
+      }
     }
   }
   __syncthreads();
+  if (tid < G) {  // the CTA's statistics: maximum, rounded and unrounded sums
+    float L = 0.f, E = 0.f;
+    for (int k = 0; k < nblk; ++k) {
+      L += sB[(G + tid) * 8 + k];
+      E += sB[(2 * G + tid) * 8 + k];
+    }
+    s_M[tid] = tid == 0 ? M[0] : M[G - 1];
+    s_L[tid] = L;
+    s_E[tid] = E;
+  }
 
   // ---- O = P V: warp w takes head-dimension columns [w D / 8, (w + 1) D / 8)
   {
