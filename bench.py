@@ -45,9 +45,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Runtime-mask SWA warm median at this decode shape (B=1, Hq=4, Hkv=2, D=256, W=1024, 1088
 # rows) on IBM Spyre: the only published figure for this metric and workload (other hardware).
 SPYRE_RUNTIME_MASK_US = 562.0
-# DRAM bytes (read + write) of one launch of the dominant kernel, decode_kernel<256, 2, 16>, from
-# one ncu capture of the current kernel (cold cache); set to None whenever that kernel changes.
-DECODE_TRAFFIC_BYTES = 2299648
+# The dominant kernel of the bench step and the committed summary of its ncu capture; the summary
+# records the DRAM bytes of one launch and the SHA-256 of the kernel source it was taken on, and the
+# bench reports that traffic only while the source is unchanged (else null).
+DOMINANT_KERNEL = "decode_small_kernel<256, 2>"
+DOMINANT_SOURCE = os.path.join("sliding_window_gqa_swa_gb300", "csrc", "decode_small_sm103.cu")
+DOMINANT_PROFILE = os.path.join("profiles", "decode_small_kernel_single_stream.md")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -136,6 +139,66 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def profiled_traffic():
+    """(DRAM bytes per launch, source) of the dominant kernel from its committed ncu summary, or
+    (None, reason) when there is none or the kernel source changed since the capture."""
+    import hashlib
+    try:
+        src = open(os.path.join(ROOT, DOMINANT_SOURCE), "rb").read()
+        text = open(os.path.join(ROOT, DOMINANT_PROFILE)).read()
+    except OSError:
+        return None, "no ncu summary of the current kernel"
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    try:
+        nbytes = int(fields["traffic_bytes_per_launch"])
+        sha = fields["kernel_source_sha256"]
+    except (KeyError, ValueError):
+        return None, "ncu summary without a traffic line"
+    if hashlib.sha256(src).hexdigest() != sha:
+        return None, "kernel changed since the ncu capture"
+    return nbytes, DOMINANT_PROFILE
+
+
+def host_threads():
+    """Host cores and the BLAS thread count NumPy's matrix products use (best effort)."""
+    info = {"cores": os.cpu_count()}
+    try:
+        import threadpoolctl
+        pools = threadpoolctl.threadpool_info()
+        blas = [p_["num_threads"] for p_ in pools if p_.get("user_api") == "blas"]
+        if blas:
+            info["blas_threads"] = int(max(blas))
+            return info
+    except Exception:
+        pass
+    try:  # the OpenBLAS that NumPy loaded, asked directly
+        import ctypes
+        libs = set()
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1] if line.split() else ""
+                if "openblas" in os.path.basename(path).lower():
+                    libs.add(path)
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                         "openblas_get_num_threads", "scipy_openblas_get_num_threads"):
+                fn = getattr(lib, name, None)
+                if fn is not None:
+                    info["blas_threads"] = int(fn())
+                    return info
+    except Exception:
+        pass
+    env = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    info["blas_threads"] = int(env) if env else None
+    return info
+
+
 def admitted_pairs(seq_len: int, window: int, pad: int, img) -> int:
     """Admitted pairs per head of one padded sequence with image blocks: a
     query q >= pad sees keys [max(pad, q - W + 1), q], extended to the end of
@@ -175,7 +238,11 @@ class SingleStreamJob:
         self.scale = self.D ** -0.5
         place = (lambda t: t.pin_memory()) if e2e else (lambda t: t.to(dev))
         self.pq, self.pk, self.pv = place(c.prompt_q), place(c.prompt_k), place(c.prompt_v)
-        self.dq, self.dk, self.dv = place(c.dec_q), place(c.dec_k), place(c.dec_v)
+        # each decode step's q, k_new and v_new for all layers, packed in one row so the step
+        # stages its inputs with one copy
+        T = c.steps
+        self.nq, self.nk = c.dec_q[0].numel(), c.dec_k[0].numel()
+        self.dec = place(torch.cat([c.dec_q.reshape(T, -1), c.dec_k.reshape(T, -1), c.dec_v.reshape(T, -1)], 1))
         if e2e:
             self.d_pq = torch.empty(c.prompt_q.shape, dtype=torch.bfloat16, device=dev)
             self.d_pk = torch.empty(c.prompt_k.shape, dtype=torch.bfloat16, device=dev)
@@ -192,10 +259,11 @@ class SingleStreamJob:
         self.meta = swa.Meta(self.B, self.S, 0, self.S, self.W)
         self.mask = torch.empty(self.B, self.cmp.rows, dtype=torch.uint8, device=dev)
         self.ws = swa.decode_workspace(self.cmp, self.Hq)
-        # staging buffers the captured step graph reads and writes
-        self.qb = torch.empty((self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
-        self.kb = torch.empty((self.L, self.B, self.Hkv, self.D), dtype=torch.bfloat16, device=dev)
-        self.vb = torch.empty_like(self.kb)
+        # staging buffers the captured step graph reads (views of one buffer) and writes
+        self.stage = torch.empty(self.nq + 2 * self.nk, dtype=torch.bfloat16, device=dev)
+        self.qb = self.stage[:self.nq].view(self.L, self.B, self.Hq, self.D)
+        self.kb = self.stage[self.nq:self.nq + self.nk].view(self.L, self.B, self.Hkv, self.D)
+        self.vb = self.stage[self.nq + self.nk:].view(self.L, self.B, self.Hkv, self.D)
         self.ob = torch.empty((self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
         self.graph = None
         self.rolls = 0 if ring else (self.T - 1) // 64
@@ -203,7 +271,7 @@ class SingleStreamJob:
         # (mask + one decode per layer) per step, rolls
         self.launches = 2 + 2 * self.L + 1 + self.T * (1 + self.L) + self.rolls
         self.h2d_bytes = (c.prompt_q.numel() + c.prompt_k.numel() + c.prompt_v.numel()
-                          + c.dec_q.numel() + c.dec_k.numel() + c.dec_v.numel()) * 2 if e2e else 0
+                          + self.dec.numel()) * 2 if e2e else 0
         self.d2h_bytes = self.outs.numel() * 2 if e2e else 0
 
     def _capture(self):
@@ -242,9 +310,7 @@ class SingleStreamJob:
         for t in range(self.T):
             if self.cmp.needs_roll():
                 swa.roll(self.cmp)
-            self.qb.copy_(self.dq[t], non_blocking=True)
-            self.kb.copy_(self.dk[t], non_blocking=True)
-            self.vb.copy_(self.dv[t], non_blocking=True)
+            self.stage.copy_(self.dec[t], non_blocking=True)
             if self.l2_flush is not None:
                 self.l2_flush.fill_(t & 127)
             e["step_s"][t].record()
@@ -308,6 +374,7 @@ def run_ours(args):
     dec_bytes = (job.W * job.B * job.Hkv * job.D * 2 * 2
                  + job.B * (2 * job.Hq + 2 * job.Hkv) * job.D * 2 + job.B * job.cmp.rows)
     achieved_gbs = dec_bytes / (launch_us * 1e-6) / 1e9
+    traffic, traffic_src = profiled_traffic()
     pre_flops = 4.0 * job.D * job.Hq * causal_pairs(job.S, job.W) * job.B * L
     pre_tflops = pre_flops / (prefill_ms / args.steps * 1e-3) / 1e12
     launches = job.launches * args.steps
@@ -405,11 +472,12 @@ def run_ours(args):
         "decode_launch_us": round(launch_us, 4),
         "prefill_ms_per_job": round(prefill_ms / args.steps, 3),
         "prefill_tflops": round(pre_tflops, 2),
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel<256,2>", "achieved": round(achieved_gbs, 1),
+        "roofline": {"bound": "hbm", "kernel": DOMINANT_KERNEL, "achieved": round(achieved_gbs, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved_gbs / peaks["hbm_gbs"], 4),
-                     "traffic": DECODE_TRAFFIC_BYTES, "peak_source": peaks_src,
+                     "traffic": traffic, "traffic_source": traffic_src, "peak_source": peaks_src,
                      "per_launch_bytes": int(dec_bytes),
-                     "note": "launch duration = per-step graph time (shared mask + 26 decodes) / 26"},
+                     "note": "launch duration = per-step graph time (shared mask + 26 decodes) / 26; the working "
+                             "set is L2-resident within a step, so the kernel is latency-bound"},
         "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -421,7 +489,17 @@ def run_ours(args):
 
 
 # ----------------------------------------------------------------------------- secondary workloads
-def run_secondary(swa, synth, dev, peaks, training_docs=4):
+def oracle_rate(fn, seconds: float, max_calls: int = 100000):
+    """Seconds per call of ``fn`` (the fp64 oracle on one sample unit), timed over about ``seconds``."""
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_calls and (n == 0 or time.perf_counter() - t0 < seconds):
+        fn(n)
+        n += 1
+    return (time.perf_counter() - t0) / n, n
+
+
+def run_secondary(swa, synth, dev, peaks, training_docs=4, oracle_seconds=4.0):
     out = {}
     for name, fn in (("batched_decode", bench_batched_decode), ("chunked_vlm_prefill", bench_vlm_prefill),
                      ("packed_prefill_d512", bench_packed),
@@ -431,7 +509,74 @@ def run_secondary(swa, synth, dev, peaks, training_docs=4):
         except Exception as e:  # reported in the line, never hidden
             out[name] = {"error": repr(e)}
         torch.cuda.empty_cache()
+    if oracle_seconds > 0:
+        for name, fn in (("batched_decode", oracle_batched_decode), ("chunked_vlm_prefill", oracle_vlm_prefill),
+                         ("packed_prefill_d512", oracle_packed)):
+            if name in out and "error" not in out[name]:
+                try:
+                    out[name]["cpu_baseline"] = fn(synth, oracle_seconds)
+                except Exception as e:
+                    out[name]["cpu_baseline"] = {"error": repr(e)}
     return out
+
+
+def oracle_batched_decode(synth, seconds):
+    """The fp64 oracle on (sequence, step) queries of the batched decode workload, scaled to one step of
+    all 64 sequences (every query head of a sequence per call)."""
+    from oracle import reference
+    c = synth.workload3(steps=256)
+    B, W, D, S = c.batch, c.window, c.head_dim, c.prompt_len
+
+    def one(n):
+        b, t = n % B, (n // B) % c.steps
+        reference.decode_full(c.prompt_k[0][b:b + 1], c.prompt_v[0][b:b + 1], c.dec_q[:, 0, b:b + 1],
+                              c.dec_k[:, 0, b:b + 1], c.dec_v[:, 0, b:b + 1], S, W, D ** -0.5,
+                              c.valid_start[b:b + 1].numpy(), steps=[t])
+    sec, n = oracle_rate(one, seconds)
+    th = host_threads()
+    return {"value": round(sec * B * 1e6, 1), "unit": "us/step", "cores": th["cores"],
+            "blas_threads": th.get("blas_threads"), "kind": "oracle",
+            "sample": f"{n} (sequence, step) decode queries (16 query heads each), scaled by 64 sequences"}
+
+
+def oracle_vlm_prefill(synth, seconds):
+    """The fp64 oracle on query rows of the chunked VLM prefill (sequence 1, with the image blocks),
+    scaled to all B x S rows."""
+    from oracle import reference
+    c = synth.workload4()
+    B, S, W, D = c.batch, c.seq_len, c.window, c.head_dim
+    rows = list(range(1024, S, 97))
+
+    def one(n):
+        r = rows[n % len(rows)]
+        reference.prefill_rows(c.q, c.k, c.v, W, D ** -0.5, 1, [r], c.valid_start.numpy(), c.img_id.numpy())
+    sec, n = oracle_rate(one, seconds)
+    th = host_threads()
+    pairs = sum(admitted_pairs(S, W, int(c.valid_start[b]), c.img_id[b].numpy()) for b in range(B))
+    total_s = sec * B * S
+    return {"value": round(total_s * 1e3, 1), "unit": "ms", "tflops": round(4.0 * D * c.q_heads * pairs / total_s / 1e12, 6),
+            "cores": th["cores"], "blas_threads": th.get("blas_threads"), "kind": "oracle",
+            "sample": f"{n} query rows (8 heads each) of sequence 1, scaled to {B} x {S} rows"}
+
+
+def oracle_packed(synth, seconds):
+    """The fp64 oracle on query rows of the packed documents (D = 512), scaled to all 16384 rows."""
+    from oracle import reference
+    c = synth.workload5()
+    T, W, D = int(c.cu_seqlens[-1]), c.window, c.head_dim
+    cu = c.cu_seqlens.numpy()
+    rows = list(range(37, T, 211))
+
+    def one(n):
+        r = rows[n % len(rows)]
+        reference.varlen_rows(c.q, c.k, c.v, cu, W, D ** -0.5, [r])
+    sec, n = oracle_rate(one, seconds)
+    th = host_threads()
+    total_s = sec * T
+    pairs = 4 * causal_pairs(4096, W)
+    return {"value": round(total_s * 1e3, 1), "unit": "ms", "tflops": round(4.0 * D * c.q_heads * pairs / total_s / 1e12, 6),
+            "cores": th["cores"], "blas_threads": th.get("blas_threads"), "kind": "oracle",
+            "sample": f"{n} query rows (16 heads each), scaled to {T} rows"}
 
 
 def bench_batched_decode(swa, synth, dev, peaks, steps=256, reps=3):
@@ -657,8 +802,10 @@ def cpu_baseline(case, seconds: float):
         _oracle_decode_queries(case, 26, n)
         n += 26
     el = time.perf_counter() - t0
-    return {"value": round(el * 1e6 / n, 1), "unit": "us/layer", "cores": torch.get_num_threads(),
-            "kind": "oracle", "sample": f"{n} (step, layer) decode queries of the single-stream workload, fp64 NumPy"}
+    th = host_threads()
+    return {"value": round(el * 1e6 / n, 1), "unit": "us/layer", "cores": th["cores"],
+            "blas_threads": th.get("blas_threads"), "kind": "oracle",
+            "sample": f"{n} (step, layer) decode queries of the single-stream workload, fp64 NumPy"}
 
 
 def run_reference(args):
@@ -675,7 +822,7 @@ def run_reference(args):
         _oracle_decode_queries(case, per, (args.warmup + k) * per)
     tot = time.perf_counter() - t0
     us = tot * 1e6 / (per * args.steps)
-    cores = torch.get_num_threads()
+    cores = host_threads()["cores"]
     line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot * 1e3 / args.steps, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

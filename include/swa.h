@@ -346,8 +346,11 @@ SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, 
 
 /* Largest scratch area swa_decode_noalloc can use (bytes): the device image of
  * libswa.so holds one static array of this size on every GPU that loads it,
- * until the process exits. */
+ * until the process exits.  Its first SWA_DECODE_STATIC_MAX_SLABS x 4 bytes
+ * (rounded up to 256) are ticket counters, one per (sequence, KV head) slab;
+ * the split statistics and partials follow. */
 #define SWA_DECODE_STATIC_SCRATCH_BYTES (8u << 20)
+#define SWA_DECODE_STATIC_MAX_SLABS 65536
 
 /* swa_decode for callers that may not allocate device memory -- for example a
  * plugin running inside an inference runtime that plans every buffer up front
@@ -355,16 +358,21 @@ SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, 
  * break the runtime's memory accounting and can synchronise the device.  The
  * pages have no counterpart to this entry point; it exists only for such
  * callers.
- * Same arguments, results and checks as swa_decode, without the workspace:
- * the split-K partials live in a static device array of
- * SWA_DECODE_STATIC_SCRATCH_BYTES.  A shape whose workspace
- * (swa_decode_workspace_bytes) is larger fails with SWA_EUNSUPPORTED.
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Each
- * call clears the array's ticket counters on `stream` before its kernel.
- * Every call on a device shares the one array and leaves the last call's
- * partials in it, so calls that overlap on the GPU (other streams, other host
- * threads) race: serialise them.  Allocates nothing. */
+ * Same arguments, results and checks as swa_decode, without the workspace.
+ * Only shapes whose splits merge through the workspace (several splits per
+ * slab that do not form one thread-block cluster: large batches, or windows
+ * longer than 16 clusters' worth of rows) use scratch; for them the ticket
+ * counters and the split partials live in the static array above, and a shape
+ * with more than SWA_DECODE_STATIC_MAX_SLABS slabs or partials that do not fit
+ * fails with SWA_EUNSUPPORTED before any CUDA call.
+ * The first call on a device does a set-up with that device current: it looks
+ * up the array's device address and clears the ticket area (a synchronous
+ * memset); make that first call before any stream capture.  Every decode
+ * leaves its slabs' tickets at zero again (also when a bounded wait gave up),
+ * so later calls need no clearing.  Every call on a device shares the one
+ * array and leaves the last call's partials in it, so calls that overlap on
+ * the GPU (other streams, other host threads) race: serialise them.
+ * Allocates nothing. */
 SWA_API swa_status swa_decode_noalloc(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
                                       const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
                                       float scale, swa_bf16* out, float* lse, swa_stream_t stream);

@@ -633,15 +633,22 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   const swa::DecodeSplit sp =
       swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
                         swa::decode_max_cluster());
-  if (sp.total > size_t(SWA_DECODE_STATIC_SCRATCH_BYTES))
-    return fail(SWA_EUNSUPPORTED, "this shape needs %zu bytes of decode scratch; the static array holds %zu",
-                sp.total, size_t(SWA_DECODE_STATIC_SCRATCH_BYTES));
+  // The static array: a fixed ticket area for up to SWA_DECODE_STATIC_MAX_SLABS
+  // (sequence, KV head) slabs, then the split statistics and partials.  Only
+  // the workspace merge (several splits that are not one cluster) uses it.
+  const size_t pairs = size_t(d.batch) * d.kv_heads;
+  const size_t tickets = swa::align256(size_t(SWA_DECODE_STATIC_MAX_SLABS) * sizeof(int32_t));
+  const size_t partials = sp.total - sp.off_ml;
+  const bool uses_scratch = sp.nsplit > 1 && !sp.cluster;
+  if (uses_scratch && (pairs > size_t(SWA_DECODE_STATIC_MAX_SLABS) ||
+                       tickets + partials > size_t(SWA_DECODE_STATIC_SCRATCH_BYTES)))
+    return fail(SWA_EUNSUPPORTED,
+                "this shape needs %zu bytes of decode scratch for %zu slabs; the static array holds %zu bytes "
+                "(tickets for %d slabs)",
+                tickets + partials, pairs, size_t(SWA_DECODE_STATIC_SCRATCH_BYTES), SWA_DECODE_STATIC_MAX_SLABS);
   void* scratch = nullptr;
-  cudaError_t e = swa::decode_static_scratch(&scratch);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-  // the tickets must start at zero
-  e = cudaMemsetAsync(scratch, 0, sp.off_ml, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(decode scratch tickets)");
+  cudaError_t e = swa::decode_static_scratch(&scratch);  // first call on a device: address and cleared tickets
+  if (e != cudaSuccess) return cuda_fail(e, "decode static scratch set-up");
   swa::DecodeArgs a;
   a.q = q;
   a.k_new = k_new;
@@ -654,8 +661,8 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   a.lse = lse;
   char* ws = static_cast<char*>(scratch);
   a.counters = reinterpret_cast<int32_t*>(ws);
-  a.ws_ml = reinterpret_cast<float*>(ws + sp.off_ml);
-  a.ws_acc = reinterpret_cast<float*>(ws + sp.off_acc);
+  a.ws_ml = reinterpret_cast<float*>(ws + tickets);
+  a.ws_acc = reinterpret_cast<float*>(ws + tickets + (sp.off_acc - sp.off_ml));
   a.batch = d.batch;
   a.q_heads = q_heads;
   a.kv_heads = d.kv_heads;

@@ -622,21 +622,29 @@ decode_kernel(const DecodeArgs a) {
     return;
   }
 
-  // ---- workspace merge
-  if (aborted) return;
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int g = i / D, d = i % D;
-    a.ws_acc[((head0 + g) * nsplit + split) * D + d] = cta_acc[i];
-  }
-  if (tid < G) {
-    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 0] = s_M[tid];
-    a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 1] = s_L[tid];
+  // ---- workspace merge.  Every CTA takes a ticket, an aborted one with a
+  // mark in the upper bits, so the last CTA of the slab always resets the
+  // counter (the workspace is ready for the next call) and writes the output
+  // only when no CTA of the slab gave up.
+  if (!aborted) {
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int g = i / D, d = i % D;
+      a.ws_acc[((head0 + g) * nsplit + split) * D + d] = cta_acc[i];
+    }
+    if (tid < G) {
+      a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 0] = s_M[tid];
+      a.ws_ml[((head0 + tid) * nsplit + split) * 2 + 1] = s_L[tid];
+    }
   }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const int ticket = atomicAdd(&a.counters[b * a.kv_heads + h], 1);
-    s_last = (ticket == nsplit - 1);
+    constexpr int kAbortMark = 1 << 16;
+    const int ticket = atomicAdd(&a.counters[b * a.kv_heads + h], aborted ? 1 + kAbortMark : 1);
+    const bool last = (ticket & (kAbortMark - 1)) == nsplit - 1;
+    const bool any_abort = aborted || ticket >= kAbortMark;
+    if (last && any_abort) a.counters[b * a.kv_heads + h] = 0;
+    s_last = last && !any_abort;
   }
   __syncthreads();
   if (!s_last) return;
@@ -838,6 +846,10 @@ cudaError_t decode_static_scratch(void** ptr) {
   if (!cached[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_decode_scratch);  // with this device current
+    if (e != cudaSuccess) return e;
+    // the ticket area starts at zero (the array is zero at load; cleared once
+    // more here, synchronously); every decode leaves its tickets at zero
+    e = cudaMemset(p, 0, align256(size_t(SWA_DECODE_STATIC_MAX_SLABS) * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
     cached[dev] = p;
   }
