@@ -606,6 +606,9 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   a.cluster = sp.cluster;
   a.warps = sp.warps;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.valid_start = c->valid_start;
+  a.window = d.window;
+  a.ring = d.kind == SWA_CACHE_RING;
   cudaError_t e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return SWA_OK;
@@ -674,6 +677,9 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   a.cluster = sp.cluster;
   a.warps = sp.warps;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.valid_start = c->valid_start;
+  a.window = d.window;
+  a.ring = d.kind == SWA_CACHE_RING;
   e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return SWA_OK;

@@ -180,7 +180,27 @@ decode_kernel(const DecodeArgs a) {
   if (!append) pdl_wait();
   const uint16_t* kn = append ? a.k_new + ((long long)b * a.kv_heads + h) * D : nullptr;
   const uint16_t* vn = append ? a.v_new + ((long long)b * a.kv_heads + h) * D : nullptr;
-  const int nspec = min(kStages, nchunks);  // chunks loaded before the mask is known
+  // Chunks loaded before the mask is read: the first ones that can hold an
+  // admitted row.  In an anchored cache the admitted rows of a sequence are
+  // one interval, [max(0, valid_start - origin, cur_row - W + 1), cur_row],
+  // computed here from the state the step's mask kernel left (every kernel
+  // that writes the state completes before a decode of the step starts); in
+  // a ring cache the first chunks are taken.  Chunks before c_first are never
+  // fetched; later ones only when the mask admits one of their rows.
+  int c_first = 0, c_end = nchunks;
+  if (!a.ring && append && nchunks > kStages) {
+    const int cr = st->cur_row, org = st->origin, vs = a.valid_start[b];
+    const int lo = max(max(0, vs - org), max(-org, cr - a.window + 1)) - r0;
+    const int hi = min(min(cr, R - 1) - r0, nrows - 1);  // within this split's rows
+    if (cr < 0 || cr >= R || hi < 0 || lo >= nrows || lo > hi) {
+      c_first = c_end = 0;  // nothing of this split is admitted (or the state is off: the mask decides)
+    } else {
+      c_first = max(0, lo) / CH;
+      c_end = hi / CH + 1;
+    }
+  }
+  // chunks [c_first, c_first + nspec) are fetched early; c_end <= nchunks
+  const int nspec = max(0, min(kStages, c_end - c_first));
   // a range that fits in the ring is loaded at once by every thread with
   // 16-byte asynchronous copies (lowest latency); longer ranges stream
   // through the ring with bulk copies
@@ -209,12 +229,13 @@ decode_kernel(const DecodeArgs a) {
         mbar_arrive_expect_tx(smem_u32(&s_merge_bar), uint32_t(a.nsplit * (1 + slice) * 16));
       }
       fence_mbar_init();
-      for (int c = 0; c < (oneshot ? 0 : nspec); ++c) {
+      for (int i = 0; i < (oneshot ? 0 : nspec); ++i) {
+        const int c = c_first + i;
         const uint32_t bytes = uint32_t(min(CH, nrows - c * CH)) * D * 2;
-        mbar_arrive_expect_tx(bar_full0 + 8 * c, 2 * bytes);
+        mbar_arrive_expect_tx(bar_full0 + 8 * i, 2 * bytes);
         const long long row = r0 + c * CH;
-        bulk_load(sring + c * kStageBytes, Kc + row * D, bytes, bar_full0 + 8 * c);
-        bulk_load(sring + c * kStageBytes + CHUNK_BYTES, Vc + row * D, bytes, bar_full0 + 8 * c);
+        bulk_load(sring + i * kStageBytes, Kc + row * D, bytes, bar_full0 + 8 * i);
+        bulk_load(sring + i * kStageBytes + CHUNK_BYTES, Vc + row * D, bytes, bar_full0 + 8 * i);
       }
     }
     // everything above read only this layer's cache rows, which no earlier
@@ -251,7 +272,7 @@ decode_kernel(const DecodeArgs a) {
     for (int c = lane; c < nchunks; c += 32) {
       uint8_t any = 0;
       for (int i = c * CH; i < min(nrows, (c + 1) * CH); ++i) any |= mask_s[i];
-      chunk_on[c] = oneshot || (c < nspec) || (state_ok && any);
+      chunk_on[c] = oneshot || (c >= c_first && c < c_first + nspec) || (c >= c_first + nspec && state_ok && any);
     }
   }
   if (!state_ok) {
@@ -264,7 +285,7 @@ decode_kernel(const DecodeArgs a) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int idx = nspec;
-      for (int c = nspec; c < nchunks; ++c) {
+      for (int c = c_first + nspec; c < nchunks; ++c) {
         if (!chunk_on[c]) continue;
         const int s = idx % kStages;
         if (!wait_bar(bar_empty0 + 8 * s, ((idx / kStages) & 1) ^ 1, abort_flag, &st->error)) break;

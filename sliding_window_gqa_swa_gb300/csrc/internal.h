@@ -118,6 +118,9 @@ struct DecodeArgs {
   int cluster;            // 1: the splits of a slab form one cluster and merge in shared memory
   int warps;              // compute warps per CTA: 8 (throughput) or 16 (latency)
   float scale_log2;       // scale * log2(e)
+  const int32_t* valid_start;  // [B] left-pad counts (the cache's copy)
+  int window;
+  int ring;               // 1: modular ring cache (rows hold positions p - ((p - r) mod W))
 };
 
 // Split choice and workspace size shared by the host API and the launcher.
