@@ -118,20 +118,6 @@ Layout layout_of(const swa_cache_desc& d) {
   return l;
 }
 
-int sm_count_of_current_device() {
-  static std::mutex mu;
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-  std::lock_guard<std::mutex> lock(mu);
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 bool check_meta(const swa_prefill_meta* m) {
   if (!m) {
     fail(SWA_EINVAL, "meta is NULL");
@@ -553,7 +539,7 @@ size_t swa_decode_workspace_bytes(const swa_cache* c, int32_t q_heads) {
     return 0;
   }
   const swa_cache_desc& d = c->desc;
-  return swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+  return swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, swa::device_sm_count(),
                         swa::decode_max_cluster()).total;
 }
 
@@ -578,7 +564,7 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
   if (c->cur_row < 0) return fail(SWA_ESTATE, "build the step's decode mask before decoding");
   const swa::DecodeSplit sp =
-      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, swa::device_sm_count(),
                         swa::decode_max_cluster());
   if (ws_bytes < sp.total) return fail(SWA_EINVAL, "workspace too small (%zu < %zu)", ws_bytes, sp.total);
   swa::DecodeArgs a;
@@ -634,7 +620,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   if (!std::isfinite(scale)) return fail(SWA_EINVAL, "scale must be finite");
   if (c->cur_row < 0) return fail(SWA_ESTATE, "build the step's decode mask before decoding");
   const swa::DecodeSplit sp =
-      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, sm_count_of_current_device(),
+      swa::decode_split(d.batch, q_heads, d.kv_heads, d.head_dim, d.rows, swa::device_sm_count(),
                         swa::decode_max_cluster());
   // The static array: a fixed ticket area for up to SWA_DECODE_STATIC_MAX_SLABS
   // (sequence, KV head) slabs, then the split statistics and partials.  Only

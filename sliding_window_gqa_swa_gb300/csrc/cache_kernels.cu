@@ -7,9 +7,26 @@
 // window + 64 anchored buffers; every 64 decode tokens the rows shift down by
 // a fixed offset with device-to-device copies).
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace swa {
+
+int device_sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 namespace {
 
 __global__ void init_state_kernel(swa_device_state* st, int32_t* vs_dst, const int32_t* vs_src,
@@ -114,7 +131,8 @@ roll_kernel(uint4* __restrict__ k, uint4* __restrict__ v, long long slabs, int r
 
 int grid_for(long long n, int threads) {
   long long g = (n + threads - 1) / threads;
-  if (g > 152LL * 64) g = 152LL * 64;
+  const long long cap = 64LL * device_sm_count();  // grid-stride loops: 64 CTAs per SM at most
+  if (g > cap) g = cap;
   return g < 1 ? 1 : int(g);
 }
 

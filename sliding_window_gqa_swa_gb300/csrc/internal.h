@@ -123,6 +123,9 @@ struct DecodeArgs {
   int ring;               // 1: modular ring cache (rows hold positions p - ((p - r) mod W))
 };
 
+// SMs of the current device (cached per device; 152 if the query fails).
+int device_sm_count();
+
 // Split choice and workspace size shared by the host API and the launcher.
 struct DecodeSplit {
   int nsplit, rows_per_split, cluster, warps;
@@ -180,6 +183,11 @@ cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s);
 // True when launch_prefill_tc runs the pair kernel for these arguments and it
 // can read the chunk's keys from k_in / v_in (the chunk starts on a key tile).
 bool prefill_reads_chunk_inputs(const PrefillArgs& a);
+
+// Head size 512, even GQA group: a four-CTA cluster per (head pair, query
+// tile), one CTA pair computing S and the softmax, the other accumulating O.
+cudaError_t launch_prefill_split512(const PrefillArgs& a, cudaStream_t s);
+bool prefill_split512_eligible(const PrefillArgs& a);
 
 // 4-D bf16 tensor map with a {64, box_rows, 1, 1} box and 128-byte swizzle
 // (dims innermost first, strides in bytes of dims 1..3); false on failure.

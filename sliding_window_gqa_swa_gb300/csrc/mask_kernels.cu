@@ -258,7 +258,7 @@ cudaError_t launch_prefill_plan(const swa_prefill_meta& meta, void* plan, cudaSt
 cudaError_t launch_dense_debug(const swa_prefill_meta& meta, uint8_t* out, cudaStream_t s) {
   const long long n = (long long)meta.batch * meta.chunk_len * meta.seq_len;
   long long g = (n + 255) / 256;
-  if (g > 152LL * 32) g = 152LL * 32;
+  if (g > 32LL * device_sm_count()) g = 32LL * device_sm_count();
   if (g < 1) g = 1;
   dense_debug_kernel<<<int(g), 256, 0, s>>>(meta, out);
   return cudaGetLastError();

@@ -168,34 +168,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// (a0, a1) * (s, s) + (b, b) on a packed fp32 pair
-__device__ __forceinline__ void fma2(float& x0, float& x1, float s, float b) {
-  uint64_t x, ss, bb;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
-  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x) : "l"(ss), "l"(bb));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x));
-}
-
-// acc += (x0, x1) on a packed fp32 pair; pair_sum gives lo + hi
-__device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
-  uint64_t x;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(x));
-}
-__device__ __forceinline__ float pair_sum(uint64_t x) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
-  return lo + hi;
-}
-
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
 // One work item: query tile qt (128 rows) of sequence b for the head pair

@@ -151,6 +151,34 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded wait of the single thread on the critical path (the MMA issuer,
+// the forwarder): polled with test_wait, because a thread suspended in
+// try_wait can resume well over a thousand SM clocks after the phase
+// completed.  kCluster: the phase completes by the peer's relaxed arrival,
+// so the successful test is followed by an acquire fence at cluster scope.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
+  auto poll = [&] {
+    if (!kCluster) return mbar_test_wait(bar, parity);
+    if (!mbar_test_wait_relaxed_cluster(bar, parity)) return false;
+    fence_acquire_cluster();
+    return true;
+  };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (poll()) return true;
+    if ((it & 255) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        if (err) atomicCAS(err, 0, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -391,17 +419,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int sv = idx % NST;
           // P_j written (so S_j read), V_j and K_{j+2} loaded: one round of polls,
           // then bounded waits for whatever is still pending
-          bool rdy = mbar_try_wait_cluster(bars.p_full(sb), (j >> 1) & 1) &&
-                     mbar_try_wait(bars.full(sv), (idx / NST) & 1);
-          for (int part = 0; next && rdy && part < KSLOTS; ++part)
-            rdy = mbar_try_wait(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1);
-          if (!rdy) {
-            ok = wait_bar<true>(bars.p_full(sb), (j >> 1) & 1, abort_flag, err) &&
-                 wait_bar(bars.full(sv), (idx / NST) & 1, abort_flag, err);
-            for (int part = 0; next && ok && part < KSLOTS; ++part)
-              ok = wait_bar(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1, abort_flag, err);
-            if (!ok) break;
-          }
+          ok = wait_spin<true>(bars.p_full(sb), (j >> 1) & 1, abort_flag, err) &&
+               wait_spin<false>(bars.full(sv), (idx / NST) & 1, abort_flag, err);
+          for (int part = 0; next && ok && part < KSLOTS; ++part)
+            ok = wait_spin<false>(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1, abort_flag, err);
+          if (!ok) break;
           tc_fence_after();
           const uint32_t ks[2] = {sKV + ((idx + 1) % NST) * LY::SLOT, sKV + ((idx + 2) % NST) * LY::SLOT};
           const uint32_t vslot = sKV + sv * LY::SLOT;
@@ -491,13 +513,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     } else if (kSm2 && n > 0 && !issuer) {
       // the peer CTA forwards each P_j's readiness to the issuing CTA with one
-      // cluster-scope arrival
-      bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
-        ok = __all_sync(0xffffffffu, wait_bar(bars.p_full(j & 1), (j >> 1) & 1, abort_flag, err));
-        if (ok && lane == 0) mbar_arrive_remote(map_shared(bars.p_full(j & 1), 0));
-        __syncwarp();
+      // relaxed cluster-scope arrival: the softmax threads finished their
+      // tensor-memory stores before arriving locally, and the issuer's
+      // successful poll is followed by an acquire fence at cluster scope
+      if (lane == 0) {
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          ok = wait_spin<false>(bars.p_full(j & 1), (j >> 1) & 1, abort_flag, err);
+          if (ok) mbar_arrive_remote_relaxed(map_shared(bars.p_full(j & 1), 0));
+        }
       }
+      __syncwarp();
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ exchange forwarder (head size 512)
@@ -828,6 +854,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   if (a.head_dim == 256)
     return (a.q_heads / a.kv_heads) % 2 == 0 ? launch_prefill_pair256(a, s) : launch_prefill_t128(a, s);
+  if (prefill_split512_eligible(a)) return launch_prefill_split512(a, s);
   const uint64_t D = uint64_t(a.head_dim);
   CUtensorMap mq, mk, mv;
   // query heads 2g and 2g + 1 share a KV head when the group size is even:

@@ -129,6 +129,21 @@ __device__ __forceinline__ void st_async_u32x4(uint32_t addr, uint32_t a, uint32
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
                : "memory");
 }
+// 4-byte variant of st_async_u32x4.
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t a, uint32_t bar) {
+  asm volatile("st.async.weak.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
+               "r"(bar)
+               : "memory");
+}
+// Bulk copy from this CTA's shared memory into another CTA's (cluster
+// addresses `dst` and `bar`), counted as transaction bytes on that CTA's
+// mbarrier.  Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier (remote) shared-memory writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
@@ -200,6 +215,33 @@ __device__ __forceinline__ void fence_acquire_cluster() { asm volatile("fence.ac
 // proxy (the tensor core reads its operands through it).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ packed fp32 arithmetic
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (x0, x1) * (s, s) + (b, b) on a packed fp32 pair
+__device__ __forceinline__ void fma2(float& x0, float& x1, float s, float b) {
+  uint64_t x, ss, bb;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ss) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(x) : "l"(ss), "l"(bb));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x0), "=f"(x1) : "l"(x));
+}
+// acc += (x0, x1) on a packed fp32 pair; pair_sum gives lo + hi
+__device__ __forceinline__ void add2(uint64_t& acc, float x0, float x1) {
+  uint64_t x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(x));
+}
+__device__ __forceinline__ float pair_sum(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo + hi;
 }
 
 // ------------------------------------------------------------------ register split
