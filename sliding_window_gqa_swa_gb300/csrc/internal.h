@@ -176,7 +176,9 @@ struct PrefillArgs {
 // Tensor-core (tcgen05) prefill.  Head size 256: the two query heads of a
 // KV head share a CTA pair on 128-key tiles when the group size is even
 // (launch_prefill_pair256), else one CTA per head on 128-key tiles
-// (launch_prefill_t128).  Head size 512: CTA pairs on 64-key tiles.
+// (launch_prefill_t128).  Head size 512: four-CTA clusters on 128-key tiles
+// for an even group (launch_prefill_split512), else column pairs on 64-key
+// tiles.
 cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_t128(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_prefill_pair256(const PrefillArgs& a, cudaStream_t s);

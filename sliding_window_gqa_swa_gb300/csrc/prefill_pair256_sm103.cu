@@ -294,7 +294,10 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     int idx = 0, qn = 0;
     auto load = [&](int kt, bool is_v, int hk, int b) {
       const int s = idx % NST;
-      ok = __all_sync(0xffffffffu, wait_bar<false>(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
+      // polled by one lane: a suspended wait resumes late and eats the ring's lookahead
+      bool got = true;
+      if (lane == 0) got = wait_spin<false>(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err);
+      ok = __shfl_sync(0xffffffffu, got, 0);
       if (ok && lane == 0) {
         int k0 = kt * BN;
         const uint32_t dst = sRing + s * SLOT;
@@ -489,7 +492,8 @@ prefill_pair256_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
       float m_run = -CUDART_INF_F, l_run = 0.f, l_exact = 0.f;
       for (int t = 0; t < n; ++t) {
         const int tt = T + t, sb = tt & 1;
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar<true>(bars.s_full(sb), (tt >> 1) & 1, abort_flag, err));
+        // polled: a suspended wait resumes late, and S is on the critical path
+        if (ok) ok = __all_sync(0xffffffffu, wait_spin<true>(bars.s_full(sb), (tt >> 1) & 1, abort_flag, err));
         if (ok) tc_fence_after();
         const uint32_t tS = tmem + lane_off + TM_S + sb * BN;
         // this group's keys [k0, k0 + 64): columns outside the row's interval are masked

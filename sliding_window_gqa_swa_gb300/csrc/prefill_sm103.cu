@@ -1,26 +1,17 @@
 // Prefill attention on the 5th-generation tensor cores (tcgen05) on 64-key
-// tiles, for head size 512 (head size 256 runs prefill_pair256_kernel or
+// tiles, for head size 512 and an odd GQA group (an even group runs
+// prefill_split512_kernel; head size 256 runs prefill_pair256_kernel or
 // prefill128_kernel).
 //
-// One CTA computes 128 query rows of one query head, over a 256-column slice
-// of the head dimension, against the key tiles (64 keys each) its rows need;
-// the tile range comes from the causal arithmetic or from the plan built on
-// the device (generic plan: image blocks, documents).  Two shapes:
-//   * head pair (kSm2, kWide: even GQA group): the two CTAs of a cluster are
-//     query heads 2g and 2g + 1 of one KV head and share every MMA
-//     (cta_group::2, M = 256).  Each CTA loads half of every K tile (32 keys)
-//     and half of every V tile (128 head-dimension columns).  Tensor memory
-//     per CTA: O (256 columns of one column half; consecutive clusters take
-//     the two halves and both compute S over the whole contraction) and two S
-//     buffers, each the lo and hi partials of two MMA chains over the halves
-//     of the contraction; P (bf16 pairs) overwrites its S columns and is the
-//     A operand of PV from tensor memory; Q stays in shared memory;
-//   * column pair (kPair: odd group): the two CTAs of a cluster hold the two
-//     256-column halves of the head; each computes a partial S over its half
-//     of the contraction and sends it into one of the peer's two exchange
-//     buffers with asynchronous remote stores; both add the two partials
-//     (fp32 addition commutes: the same S bit for bit), run the identical
-//     softmax, and accumulate their own half of O -- no MMA is done twice.
+// A cluster of two CTAs computes 128 query rows of one query head against the
+// key tiles (64 keys each) its rows need; the tile range comes from the causal
+// arithmetic or from the plan built on the device (generic plan: image
+// blocks, documents).  The two CTAs hold the two 256-column halves of the
+// head (a column pair): each computes a partial S over its half of the
+// contraction and sends it into one of the peer's two exchange buffers with
+// asynchronous remote stores; both add the two partials (fp32 addition
+// commutes: the same S bit for bit), run the identical softmax, and
+// accumulate their own half of O -- no MMA is done twice.
 // Warp roles:
 //   warp 0     TMA producer: K and V slices into a ring of slots (128-byte
 //              swizzled, 64-column boxes), in the order the MMA thread
@@ -28,18 +19,15 @@
 //   warp 1     one thread issues the MMAs: S_0 .. S_{NS-1}, then for each
 //              tile j one group that interleaves O += P_j V_j (4 MMAs, V read
 //              MN-major) with S_{j+NS} = Q K_{j+NS}^T (16 MMAs of N = 64) into
-//              the S buffer S_j came from.  The tensor pipe runs consecutive
-//              MMAs of one accumulator back to back only when the MMA is
-//              wide; interleaving the two independent chains keeps it busy.
-//              (kSm2: the odd CTA's warp 1 forwards "P_j written" to the
-//              issuing CTA; kPair: warp 10 forwards "exchange buffer read");
+//              the S buffer S_j came from;
 //   warps 2-9  softmax: two warpgroups, one query row per thread (its TMEM
 //              lane); group g owns score columns [32g, 32g + 32) of each tile
 //              and output columns [128g, 128g + 128).  Per tile: apply the
 //              row's key interval [lo, hi], take the row maximum, online
 //              softmax in the exp2 domain with lazy rescaling of O (only when
 //              the maximum grows by more than 2^8), write P (bf16); finally
-//              normalise O and store it.
+//              normalise O and store it;
+//   warp 10    forwards "exchange buffer read" to the peer.
 // Every wait is bounded; a timeout sets the device error word, makes all
 // roles stop, lets in-flight copies and MMAs finish, and frees TMEM.
 //
@@ -67,35 +55,24 @@ using namespace ptx;
 constexpr int BM = kPlanBM;    // 128 query rows per CTA
 constexpr int BN = 64;         // keys per tile
 constexpr int HS = 256;        // head-dimension slice per CTA
-// TMA warp, MMA warp, two softmax warpgroups; head size 512 adds a warp that
-// forwards the partial-score exchange's "buffer consumed" signal to the peer
-constexpr int threads_of(bool pair) { return pair ? 352 : 320; }
+// TMA warp, MMA warp, two softmax warpgroups and a warp that forwards the
+// partial-score exchange's "buffer consumed" signal to the peer
+constexpr int THREADS = 352;
 constexpr int KV_CHUNK = BN * 128;  // one 64-column box of K or V: 8 KB
 constexpr int KV_BYTES = KV_CHUNK * (HS / 64);
 constexpr int P_BYTES = BM * BN * 2;
-constexpr int Q_CHUNK = BM * 128;  // one 64-column box of Q: 16 KB
 constexpr int XS_BYTES = BM * BN * 4;  // one partial-S exchange buffer (head size 512; two of them)
 
-// kSm2: the CTA pair shares its MMAs (cta_group::2) and each CTA holds half
-// of every K/V tile: 32 keys of K (one slot per 256 contraction columns), 128
-// head-dimension columns of V (one slot).  Its whole Q row tile (the
-// contraction, 256 or 512 columns: kWide) stays in shared memory; tensor
-// memory holds O and two S buffers, each split into the partial sums over the
-// two halves of the contraction, and P overwrites the S columns it came from.
-template <bool kPair, bool kSm2, bool kWide>
+// Shared memory: the K/V ring, two P buffers, two exchange buffers, the
+// row-maximum exchange, barriers.  Q lives in tensor memory.
 struct Layout {
-  static constexpr int HQK = kWide ? 2 * HS : HS;                // contraction columns per CTA
-  static constexpr int Q_BYTES = Q_CHUNK * (HQK / 64);
-  static constexpr int SLOT = kSm2 ? KV_BYTES / 2 : KV_BYTES;    // one ring slot
-  static constexpr int KSLOTS = kWide ? 2 : 1;                   // ring slots of one K tile
-  static constexpr int NST = kPair ? 4 : 6;                      // ring slots
+  static constexpr int SLOT = KV_BYTES;                          // one ring slot
+  static constexpr int NST = 4;                                  // ring slots
   static constexpr int NS = 2;                                   // S buffers in TMEM
-  static constexpr int SB = kSm2 ? 2 * BN : BN;                  // TMEM columns of one S buffer
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + (kSm2 ? Q_BYTES : 0);
+  static constexpr int OFF_KV = 0;
   static constexpr int OFF_P = OFF_KV + NST * SLOT;
-  static constexpr int OFF_XS = OFF_P + (kSm2 ? 0 : 2 * P_BYTES);
-  static constexpr int OFF_PMAX = OFF_XS + (kPair ? 2 * XS_BYTES : 0);  // [2 groups][128 rows] fp32
+  static constexpr int OFF_XS = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_PMAX = OFF_XS + 2 * XS_BYTES;  // [2 groups][128 rows] fp32
   static constexpr int OFF_BAR = OFF_PMAX + 2 * BM * 4;
   static constexpr int N_BARS = 2 * NST + 15;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
@@ -103,13 +80,10 @@ struct Layout {
   static_assert(SMEM <= 232448, "shared memory budget");
 };
 
-// TMEM columns: O, then the S buffers (TM_S + b * SB), then the Q slice when
-// it lives in tensor memory (column pair: after two S buffers)
+// TMEM columns: O, then the S buffers (TM_S + b * BN), then the Q slice
 constexpr uint32_t TM_O = 0, TM_S = HS, TM_Q = HS + 2 * BN, TM_COLS = 512;
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, false);
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, HS, true);
-constexpr uint32_t IDESC_QK2 = idesc_bf16_f32(2 * BM, BN, false);  // CTA pair: 256 query rows
-constexpr uint32_t IDESC_PV2 = idesc_bf16_f32(2 * BM, HS, true);
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 static_assert(TM_Q + HS / 2 <= TM_COLS && TM_S + 2 * (2 * BN) <= TM_COLS, "TMEM budget");
@@ -141,34 +115,6 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   for (uint32_t it = 1;; ++it) {
     if (poll()) return true;
     if ((it & 63) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kTimeoutNs) {
-        *abort_flag = 1;
-        if (err) atomicCAS(err, 0, kErrTimeout);
-        return false;
-      }
-    }
-  }
-}
-
-// Bounded wait of the single thread on the critical path (the MMA issuer,
-// the forwarder): polled with test_wait, because a thread suspended in
-// try_wait can resume well over a thousand SM clocks after the phase
-// completed.  kCluster: the phase completes by the peer's relaxed arrival,
-// so the successful test is followed by an acquire fence at cluster scope.
-template <bool kCluster>
-__device__ __forceinline__ bool wait_spin(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  auto poll = [&] {
-    if (!kCluster) return mbar_test_wait(bar, parity);
-    if (!mbar_test_wait_relaxed_cluster(bar, parity)) return false;
-    fence_acquire_cluster();
-    return true;
-  };
-  if (poll()) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (poll()) return true;
-    if ((it & 255) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kTimeoutNs) {
         *abort_flag = 1;
@@ -211,39 +157,28 @@ __device__ __forceinline__ float mask_max(uint32_t* sr, int kbase, int lo, int h
 
 __device__ __forceinline__ void named_sync(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
 
-template <bool kPair, bool kSm2, bool kWide>
-__global__ void __launch_bounds__(threads_of(kPair), 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  using LY = Layout<kPair, kSm2, kWide>;
-  // head size 512: a head pair (kSm2 and kWide) or a column pair (kPair)
-  static_assert(kPair != kSm2 && kSm2 == kWide, "shape");
+__global__ void __launch_bounds__(THREADS, 1)
+prefill_colpair_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const PrefillArgs a) {
+  using LY = Layout;
   constexpr int NST = LY::NST;
   constexpr int NS = LY::NS;
-  constexpr int SB = LY::SB;
-  constexpr int KSLOTS = LY::KSLOTS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + LY::OFF_Q, sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
+  const uint32_t sKV = base + LY::OFF_KV, sP = base + LY::OFF_P;
   const Bars<NST> bars{base + LY::OFF_BAR};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + LY::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + LY::OFF_MISC + 4);
   int32_t* err = a.err;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // kSm2: the cluster's two CTAs are query heads 2g and 2g + 1 of one KV head
-  // (same rows, same key tiles); the even CTA issues the pair MMAs.  kWide:
-  // consecutive clusters take the two 256-column halves of O (both compute the
-  // same S over the whole contraction)
-  const int crank = kSm2 ? int(cluster_ctarank()) : 0;
-  const bool issuer = crank == 0;
-  const int half = kPair ? int(cluster_ctarank()) : (kWide ? int(blockIdx.x >> 1) & 1 : 0);  // column half of O
+  // the cluster's two CTAs hold the two 256-column halves of query head hq
+  const int half = int(cluster_ctarank());  // column half of O
   const int peer = half ^ 1;
   const int col0 = half * HS;
-  const int hq = kPair ? int(blockIdx.x >> 1)
-                       : (kWide ? 2 * int(blockIdx.x >> 2) + crank : int(blockIdx.x));
+  const int hq = int(blockIdx.x >> 1);
   // query tiles late in a causal sequence or document have the most key tiles:
   // they are scheduled first, so the short ones fill the tail of the grid
   const int qt = int(gridDim.y - 1 - blockIdx.y), b = blockIdx.z;
@@ -278,13 +213,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), 1);
     }
-    // column pair: the softmax threads copy Q into TMEM; kSm2: both CTAs' Q
-    // tiles complete on the issuing CTA's barrier
-    mbar_init(bars.q(), kSm2 ? 1 : 256);
+    // the softmax threads copy Q into TMEM
+    mbar_init(bars.q(), 256);
     for (int i = 0; i < 2; ++i) mbar_init(bars.s_full(i), 1);
     for (int i = 0; i < 2; ++i) {
-      // kSm2: the issuing CTA also counts the one arrival its peer forwards
-      mbar_init(bars.p_full(i), kSm2 && issuer ? 257 : 256);
+      mbar_init(bars.p_full(i), 256);
       mbar_init(bars.pv_done(i), 1);
     }
     mbar_init(bars.teardown(), 1);
@@ -297,164 +230,50 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     fence_mbar_init();
   }
   if (warp == 1) {
-    if (kSm2) {
-      tmem_alloc_pair(smem_u32(tmem_slot), TM_COLS);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(smem_u32(tmem_slot), TM_COLS);
-      tmem_relinquish();
-    }
+    tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    if (kSm2) prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
   }
   tc_fence_before();
-  if (kPair || kSm2) {
-    cluster_sync();  // the peer's barriers are initialised before any remote arrive
-  } else {
-    __syncthreads();
-  }
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // ring order: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for j = 0 .. n-1 (a K
-    // tile takes KSLOTS consecutive slots)
+    // ring order: K_0 .. K_{NS-1}, then V_j, K_{j+NS} for j = 0 .. n-1; this
+    // CTA's 256 columns of each
     if (n > 0) {
       bool ok = true;
       int idx = 0;
-      if (kSm2 && lane == 0) {  // this CTA's Q rows; both tiles complete on the issuer's barrier
-        if (issuer) mbar_arrive_expect_tx(bars.q(), 2 * LY::Q_BYTES);
-        for (int c = 0; c < LY::HQK / 64; ++c)
-          tma_load_4d_pair(sQ + c * Q_CHUNK, &tm_q, map_shared(bars.q(), 0), 64 * c, i0, hq, b);
-      }
-      // part < 0: V_tile; part >= 0: contraction columns [256 part, 256 part + 256) of K_tile
-      auto load = [&](int tile, int part) {
-        const bool is_v = part < 0;
+      auto load = [&](int tile, bool is_v) {
         const int s = idx % NST;
         ok = __all_sync(0xffffffffu, wait_bar(bars.empty(s), ((idx / NST) & 1) ^ 1, abort_flag, err));
         if (ok && lane == 0) {
           const int k0 = (kt_lo + tile) * BN;
           const uint32_t dst = sKV + s * LY::SLOT;
-          if constexpr (kSm2) {
-            // this CTA's half; both halves complete on the issuing CTA's barrier
-            const uint32_t bar = map_shared(bars.full(s), 0);
-            if (issuer) mbar_arrive_expect_tx(bars.full(s), 2 * LY::SLOT);
-            if (is_v) {
-              for (int c = 0; c < 2; ++c)  // head-dimension columns col0 + [128 crank, 128 crank + 128)
-                tma_load_4d_pair(dst + c * KV_CHUNK, &tm_v, bar, col0 + 128 * crank + 64 * c, k0, hk, b);
-            } else {
-              for (int c = 0; c < HS / 64; ++c)  // keys [k0 + 32 crank, k0 + 32 crank + 32)
-                tma_load_4d_pair(dst + c * (KV_CHUNK / 2), &tm_k, bar, HS * part + 64 * c, k0 + (BN / 2) * crank,
-                                 hk, b);
-            }
-          } else {
-            mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
-            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-            for (int c = 0; c < HS / 64; ++c)
-              tma_load_4d(dst + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
-          }
+          mbar_arrive_expect_tx(bars.full(s), KV_BYTES);
+          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+          for (int c = 0; c < HS / 64; ++c) tma_load_4d(dst + c * KV_CHUNK, m, bars.full(s), col0 + 64 * c, k0, hk, b);
         }
         __syncwarp();
         ++idx;
       };
-      for (int t = 0; t < NS && t < n && ok; ++t)
-        for (int part = 0; part < KSLOTS && ok; ++part) load(t, part);
+      for (int t = 0; t < NS && t < n && ok; ++t) load(t, false);
       for (int j = 0; j < n && ok; ++j) {
-        load(j, -1);
-        if (j + NS < n)
-          for (int part = 0; part < KSLOTS && ok; ++part) load(j + NS, part);
+        load(j, true);
+        if (j + NS < n && ok) load(j + NS, false);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // one thread issues every MMA; the other lanes of the warp stay idle
-    if (n > 0 && issuer && lane == 0) {
-      bool ok = wait_bar<kSm2>(bars.q(), 0, abort_flag, err);
-      // completion of the MMAs issued so far, on `bar` of both CTAs (kSm2) or of this CTA
-      auto commit = [&](uint32_t bar) {
-        if (kSm2)
-          mma_pair_commit(bar, 0x3);
-        else
-          mma_commit(bar);
-      };
-      if constexpr (kSm2) {
-        // S_t is the sum of two independent chains of NH K=16 steps, one per
-        // half of the contraction, into the lo and hi partials of S buffer
-        // t & 1; issuing them alternately keeps two accumulations in flight.
-        constexpr int NH = LY::HQK / 32;
-        // contraction step kk: Q box kk / 4 (shared memory); K from slot part
-        // kk / 16 of the tile (32 keys, four 64-column boxes of 4 KB)
-        auto qk2 = [&](int sbuf, const uint32_t* ks, int kk) {
-          const int part = kWide ? (kk >> 4) : 0, kl = kk & 15;
-          const uint64_t bd = sdesc_sw128(ks[part] + (kl >> 2) * (KV_CHUNK / 2) + (kl & 3) * 32, 16, 1024);
-          const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * Q_CHUNK + (kk & 3) * 32, 16, 1024);
-          mma_pair_bf16_ss(tmem + TM_S + sbuf * SB + (kk >= NH ? BN : 0), ad, bd, IDESC_QK2, (kk % NH) ? 1u : 0u);
-        };
-        int idx = 0;
-        for (int t = 0; t < NS && t < n && ok; ++t) {
-          uint32_t ks[2] = {0u, 0u};
-          for (int part = 0; part < KSLOTS && ok; ++part) {
-            const int s = (idx + part) % NST;
-            ok = wait_bar(bars.full(s), ((idx + part) / NST) & 1, abort_flag, err);
-            ks[part] = sKV + s * LY::SLOT;
-          }
-          if (!ok) break;
-          tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < NH; ++k) {
-            qk2(t, ks, k);
-            qk2(t, ks, NH + k);
-          }
-          commit(bars.s_full(t));
-          for (int part = 0; part < KSLOTS; ++part) commit(bars.empty((idx + part) % NST));
-          idx += KSLOTS;
-        }
-        for (int j = 0; j < n && ok; ++j) {
-          const int sb = j & 1;
-          const bool next = j + NS < n;  // S_{j+2} goes to the buffer S_j came from
-          const int sv = idx % NST;
-          // P_j written (so S_j read), V_j and K_{j+2} loaded: one round of polls,
-          // then bounded waits for whatever is still pending
-          ok = wait_spin<true>(bars.p_full(sb), (j >> 1) & 1, abort_flag, err) &&
-               wait_spin<false>(bars.full(sv), (idx / NST) & 1, abort_flag, err);
-          for (int part = 0; next && ok && part < KSLOTS; ++part)
-            ok = wait_spin<false>(bars.full((idx + 1 + part) % NST), ((idx + 1 + part) / NST) & 1, abort_flag, err);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t ks[2] = {sKV + ((idx + 1) % NST) * LY::SLOT, sKV + ((idx + 2) % NST) * LY::SLOT};
-          const uint32_t vslot = sKV + sv * LY::SLOT;
-          const uint32_t sbase = tmem + TM_S + sb * SB;
-#pragma unroll
-          for (int p = 0; p < BN / 16; ++p) {
-            // V is [keys][head dim]: MN-major B; 64-column boxes are KV_CHUNK apart,
-            // 8-key row groups 1024 B apart.  P_j from TMEM: softmax group p / 2
-            // left its 32 keys in the first 16 columns of its 32-column slice of
-            // the lo partial; 8 columns (16 keys) per step
-            const uint64_t bd = sdesc_sw128(vslot + p * 2048, KV_CHUNK, 1024);
-            mma_pair_bf16_ts(tmem + TM_O, sbase + 32 * (p >> 1) + 8 * (p & 1), bd, IDESC_PV2,
-                             (j > 0 || p > 0) ? 1u : 0u);
-            if (next) qk2(sb, ks, NH + p);  // the hi chain does not touch P_j
-          }
-          if (next) {
-            // the lo chain overwrites P_j: issued after the last PV step (the
-            // tensor pipe executes one thread's MMAs in order)
-#pragma unroll
-            for (int k = 0; k < NH; ++k) {
-              qk2(sb, ks, k);
-              if (4 + k < NH) qk2(sb, ks, NH + 4 + k);
-            }
-            commit(bars.s_full(sb));
-          }
-          commit(bars.pv_done(sb));
-          commit(bars.empty(sv));
-          for (int part = 0; next && part < KSLOTS; ++part) commit(bars.empty((idx + 1 + part) % NST));
-          idx += 1 + (next ? KSLOTS : 0);
-        }
-      } else {
+    if (n > 0 && lane == 0) {
+      bool ok = wait_bar(bars.q(), 0, abort_flag, err);
+      auto commit = [&](uint32_t bar) { mma_commit(bar); };
       // one K=16 step of S_b = Q K^T into S buffer b; K (K-major) from ring slot
       // kslot; Q from TMEM
       auto qk_step = [&](int sbuf, uint32_t kslot, int kk) {
@@ -510,20 +329,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (next) commit(bars.empty(sk));
         idx += next ? 2 : 1;
       }
-      }
-    } else if (kSm2 && n > 0 && !issuer) {
-      // the peer CTA forwards each P_j's readiness to the issuing CTA with one
-      // relaxed cluster-scope arrival: the softmax threads finished their
-      // tensor-memory stores before arriving locally, and the issuer's
-      // successful poll is followed by an acquire fence at cluster scope
-      if (lane == 0) {
-        bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
-          ok = wait_spin<false>(bars.p_full(j & 1), (j >> 1) & 1, abort_flag, err);
-          if (ok) mbar_arrive_remote_relaxed(map_shared(bars.p_full(j & 1), 0));
-        }
-      }
-      __syncwarp();
     }
   } else if (warp >= 10) {
     // ------------------------------------------------------------ exchange forwarder (head size 512)
@@ -565,13 +370,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int bar_id = 1 + q4;  // named barrier of this quadrant's two warps
     // my row slice of the exchange buffer, and the same slice in the peer's buffer
     const uint32_t xs_row = base + LY::OFF_XS + (r * BN + cb) * 4;
-    const uint32_t xs_row_peer = kPair ? map_shared(xs_row, peer) : 0;
+    const uint32_t xs_row_peer = map_shared(xs_row, peer);
 
     const float c2 = a.scale_log2;
 
     // this group's half of the row's Q slice -> TMEM (A operand of the score MMAs);
     // 32-bit column c holds the bf16 pair (2c, 2c + 1), the lower index in the low half
-    if (!kSm2 && n > 0) {
+    if (n > 0) {
       const uint4* qrow = reinterpret_cast<const uint4*>(
           a.q + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0 + grp * (HS / 2));
 #pragma unroll
@@ -604,9 +409,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const int sb = t % NS, pb = t & 1;
-      if (ok) ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
+      if (ok) ok = __all_sync(0xffffffffu, wait_bar(bars.s_full(sb), (t / NS) & 1, abort_flag, err));
       if (ok) tc_fence_after();
-      const uint32_t tS = tmem + lane_off + TM_S + sb * SB;
+      const uint32_t tS = tmem + lane_off + TM_S + sb * BN;
       const int k0 = (kt_lo + t) * BN;
       // the masking pass runs only when some row of the warp needs it
       const bool masked = !__all_sync(0xffffffffu, (k0 >= lo) && (k0 + BN - 1 <= hi));
@@ -616,15 +421,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       {
         if (ok) {
           tmem_ld32(tS + cb, sr);
-          if constexpr (kSm2) {
-            // S = lo + hi partial sums (fp32, the same order in both CTAs of a
-            // column-half pair, so they see the same S bit for bit)
-            uint32_t hr[HC];
-            tmem_ld32(tS + BN + cb, hr);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < HC; ++c) sr[c] = __float_as_uint(__uint_as_float(sr[c]) + __uint_as_float(hr[c]));
-          } else {
+          {
             tmem_ld_wait();
             // send my partial slice into the peer's exchange buffer xb (once the
             // peer has consumed what this CTA sent there two tiles ago); the
@@ -668,7 +465,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool move = (m_run == -CUDART_INF_F) ? (mt > -CUDART_INF_F) : (mt > m_run + kRescaleLog2);
       const bool rescale = move && m_run != -CUDART_INF_F;  // O holds data relative to m_run
       if (__any_sync(0xffffffffu, rescale)) {
-        ok = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
+        ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort_flag, err));
         if (!ok) continue;
         tc_fence_after();
         const float alpha = rescale ? exp2f(m_run - mt) : 1.f;
@@ -703,13 +500,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
       l_run += ls[0] + ls[1];
       l_exact += es[0] + es[1];
-      if constexpr (kSm2) {
-        // P_t over the first 16 columns of this group's slice of the lo partial
-        // (already read); PV_{t-2}, the last reader of those columns, completed
-        // before S_t did
-        tmem_st16(tS + cb, pk);
-        tmem_st_wait();
-      } else {
+      {
         if (t >= 2) {  // P buffer pb is free once PV_{t-2} completed
           ok = __all_sync(0xffffffffu, wait_bar(bars.pv_done(pb), ((t - 2) >> 1) & 1, abort_flag, err));
           if (!ok) continue;
@@ -735,7 +526,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // epilogue: O / l -> bf16, this group's columns of the CTA's slice
     bool have_o = n > 0 && ok;
     if (have_o)
-      have_o = __all_sync(0xffffffffu, wait_bar<kSm2>(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
+      have_o = __all_sync(0xffffffffu, wait_bar(bars.pv_done((n - 1) & 1), ((n - 1) >> 1) & 1, abort_flag, err));
     tc_fence_after();
     const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
     uint16_t* orow = a.out + (((long long)b * a.chunk_len + i) * a.q_heads + hq) * a.head_dim + col0;
@@ -766,11 +557,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (*abort_flag) {
     // let the MMAs and TMA copies this CTA issued finish before TMEM and
     // shared memory are released
-    if (warp == 1 && lane == 0 && issuer) {
-      if (kSm2)
-        mma_pair_commit(bars.teardown(), 0x1);
-      else
-        mma_commit(bars.teardown());
+    if (warp == 1 && lane == 0) {
+      mma_commit(bars.teardown());
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(bars.teardown(), 0) && globaltimer_ns() - t0 < kTimeoutNs) {
       }
@@ -782,44 +570,33 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     __syncthreads();
   }
-  if (kPair || kSm2) cluster_sync();  // the peer no longer reads or writes this CTA's shared memory
+  cluster_sync();  // the peer no longer reads or writes this CTA's shared memory
   tc_fence_after();
-  if (warp == 1) {
-    if (kSm2)
-      tmem_dealloc_pair(tmem, TM_COLS);
-    else
-      tmem_dealloc(tmem, TM_COLS);
-  }
+  if (warp == 1) tmem_dealloc(tmem, TM_COLS);
 }
 
-template <bool kPair, bool kSm2, bool kWide>
-cudaError_t launch_kind(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a,
-                        cudaStream_t s) {
-  using LY = Layout<kPair, kSm2, kWide>;
+cudaError_t launch_colpair(const CUtensorMap& mk, const CUtensorMap& mv, const PrefillArgs& a, cudaStream_t s) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<kPair, kSm2, kWide>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM);
+    attr_err = cudaFuncSetAttribute(prefill_colpair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Layout::SMEM);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int nqt = (a.chunk_len + BM - 1) / BM;
   cudaLaunchConfig_t cfg = {};
-  // head size 512: two CTAs per query head (the two column halves of O)
-  cfg.gridDim = dim3(a.q_heads * (kPair || kWide ? 2 : 1), nqt, a.batch);
-  cfg.blockDim = dim3(threads_of(kPair));
-  cfg.dynamicSmemBytes = LY::SMEM;
+  // two CTAs per query head (the two column halves of O)
+  cfg.gridDim = dim3(a.q_heads * 2, nqt, a.batch);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = Layout::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
-  if (kPair || kSm2) {
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-  }
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<kPair, kSm2, kWide>, mq, mk, mv, a);
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_colpair_kernel, mk, mv, a);
 }
 
 }  // namespace
@@ -854,25 +631,17 @@ cudaError_t launch_prefill_tc(const PrefillArgs& a, cudaStream_t s) {
   if (a.head_dim != 256 && a.head_dim != 512) return cudaErrorInvalidValue;
   if (a.head_dim == 256)
     return (a.q_heads / a.kv_heads) % 2 == 0 ? launch_prefill_pair256(a, s) : launch_prefill_t128(a, s);
+  // head size 512: four-CTA clusters for an even GQA group, column pairs otherwise
   if (prefill_split512_eligible(a)) return launch_prefill_split512(a, s);
   const uint64_t D = uint64_t(a.head_dim);
-  CUtensorMap mq, mk, mv;
-  // query heads 2g and 2g + 1 share a KV head when the group size is even:
-  // their CTAs then form a pair that shares its MMAs and K/V tiles
-  const bool sm2 = (a.q_heads / a.kv_heads) % 2 == 0;
-  // K / V: dims {D, key rows, Hkv, B} with the caller's strides
+  CUtensorMap mk, mv;
+  // K / V: dims {D, key rows, Hkv, B} with the caller's strides (Q is read
+  // with 16-byte row loads into TMEM)
   const uint64_t kd[4] = {D, uint64_t(a.key_dim_rows), uint64_t(a.kv_heads), uint64_t(a.batch)};
   const uint64_t ks[3] = {uint64_t(a.key_row_stride) * 2, uint64_t(a.key_head_stride) * 2,
                           uint64_t(a.key_seq_stride > 0 ? a.key_seq_stride : a.key_dim_rows * a.key_row_stride) * 2};
-  if (!make_tmap_bf16(&mk, a.k, kd, ks, sm2 ? BN / 2 : BN) || !make_tmap_bf16(&mv, a.v, kd, ks, BN))
-    return cudaErrorInvalidValue;
-  // Q [B, C, Hq, D]: dims {D, C, Hq, B} (tiles of 128 rows; the head pair
-  // loads them with TMA, the column pair reads rows with 16-byte loads)
-  const uint64_t qd[4] = {D, uint64_t(a.chunk_len), uint64_t(a.q_heads), uint64_t(a.batch)};
-  const uint64_t qs[3] = {uint64_t(a.q_heads) * D * 2, D * 2, uint64_t(a.chunk_len) * a.q_heads * D * 2};
-  if (!make_tmap_bf16(&mq, a.q, qd, qs, BM)) return cudaErrorInvalidValue;
-  // head size 512: a head pair for an even GQA group, a column pair otherwise
-  return sm2 ? launch_kind<false, true, true>(mq, mk, mv, a, s) : launch_kind<true, false, false>(mq, mk, mv, a, s);
+  if (!make_tmap_bf16(&mk, a.k, kd, ks, BN) || !make_tmap_bf16(&mv, a.v, kd, ks, BN)) return cudaErrorInvalidValue;
+  return launch_colpair(mk, mv, a, s);
 }
 
 }  // namespace swa

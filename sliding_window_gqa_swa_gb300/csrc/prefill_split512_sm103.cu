@@ -294,6 +294,8 @@ prefill_split512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // (one lane; its waits are polled: a suspended wait resumes late and eats
+    // the ring's lookahead)
     if (n > 0 && lane == 0) {
       bool ok = true;
       if (score) {
@@ -310,7 +312,7 @@ prefill_split512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           const int k0 = (kt_lo + t) * BN + (crank & 1) * (BN / 2);
           for (int h = 0; h < 2 && ok; ++h) {
             const int u = 2 * t + h, s = u % NSTK;
-            ok = wait_bar<true>(bars.k_empty(s), ((u / NSTK) & 1) ^ 1, abort_flag, err);
+            ok = wait_spin<true>(bars.k_empty(s), ((u / NSTK) & 1) ^ 1, abort_flag, err);
             if (!ok) break;
             if (leader) mbar_arrive_expect_tx(bars.k_full(s), 2 * K_SLOT);
             for (int c = 0; c < 4; ++c)
@@ -324,7 +326,7 @@ prefill_split512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         for (int t = 0; t < n && ok; ++t) {
           for (int h = 0; h < 2 && ok; ++h) {
             const int u = 2 * t + h, s = u % NSTV;
-            ok = wait_bar<true>(bars.v_empty(s), ((u / NSTV) & 1) ^ 1, abort_flag, err);
+            ok = wait_spin<true>(bars.v_empty(s), ((u / NSTV) & 1) ^ 1, abort_flag, err);
             if (!ok) break;
             if (leader) mbar_arrive_expect_tx(bars.v_full(s), 2 * V_SLOT);
             const int k0 = (kt_lo + t) * BN + 64 * h;

@@ -79,9 +79,9 @@ CASES = {
     # size is even, and one CTA per head otherwise
     "gqa3_single_cta": (4111, 1, 6, 2, 256, 96, 260, 260, 5, None),
     "gqa4_pairs": (4112, 1, 8, 2, 256, 96, 260, 130, 5, None),
-    # head size 512: an even group runs as head pairs (two clusters per pair of
-    # heads, one per half of the output columns); an odd group as column pairs
-    # that exchange partial scores
+    # head size 512: an even group runs as four-CTA clusters (a score pair and an
+    # output pair per pair of heads); an odd group as column pairs that exchange
+    # partial scores
     "d512_gqa3_column_pairs": (4113, 1, 3, 1, 512, 64, 200, 200, 7, None),
     "d512_gqa4_pairs": (4114, 1, 8, 2, 512, 96, 260, 130, 5, None),
 }
