@@ -546,7 +546,15 @@ size_t swa_decode_workspace_bytes(const swa_cache* c, int32_t q_heads) {
 swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf16* q,
                       const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask, float scale,
                       swa_bf16* out, float* lse, void* workspace, size_t ws_bytes, swa_stream_t stream) {
+  return swa_decode_ex(c, layer, q_heads, q, k_new, v_new, mask, scale, out, lse, workspace, ws_bytes, 0u, stream);
+}
+
+swa_status swa_decode_ex(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf16* q,
+                         const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask, float scale,
+                         swa_bf16* out, float* lse, void* workspace, size_t ws_bytes, uint32_t flags,
+                         swa_stream_t stream) {
   if (!c) return fail(SWA_EINVAL, "cache is NULL");
+  if (flags & ~uint32_t(SWA_DECODE_INPUTS_READY)) return fail(SWA_EINVAL, "unknown decode flags 0x%x", flags);
   const swa_cache_desc& d = c->desc;
   if (!decodes(d.kind)) return fail(SWA_ESTATE, "decode needs a compact or ring cache");
   if (layer < 0 || layer >= d.layers) return fail(SWA_EINVAL, "layer %d out of range", layer);
@@ -595,6 +603,7 @@ swa_status swa_decode(swa_cache* c, int32_t layer, int32_t q_heads, const swa_bf
   a.valid_start = c->valid_start;
   a.window = d.window;
   a.ring = d.kind == SWA_CACHE_RING;
+  a.inputs_ready = (flags & SWA_DECODE_INPUTS_READY) && k_new ? 1 : 0;
   cudaError_t e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return SWA_OK;
@@ -666,6 +675,7 @@ swa_status swa_decode_noalloc(swa_cache* c, int32_t layer, int32_t q_heads, cons
   a.valid_start = c->valid_start;
   a.window = d.window;
   a.ring = d.kind == SWA_CACHE_RING;
+  a.inputs_ready = 0;
   e = swa::launch_decode(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return SWA_OK;

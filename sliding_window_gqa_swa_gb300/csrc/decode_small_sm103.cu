@@ -166,27 +166,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_small_kernel(const DecodeA
   }
   // everything above read only this layer's cache rows, which no earlier
   // kernel of the stream writes; the inputs below may come from the kernel
-  // launched just before this one
-  pdl_wait();
-  const int cur = st->cur_row;
-  for (int i = tid; i < nrows; i += kThreads) mask_s[i] = a.mask[(long long)b * R + r0 + i];
-  // score operand: the group's queries, lane l holding heads g = l / 4 (zero
-  // beyond G) at columns 16 kk + 2 (l % 4) + {0, 1} and + 8
+  // launched just before this one, unless the caller said they were ready
+  // before it (then they are read first and the wait overlaps their round trip)
+  int cur;
   const int gq = lane >> 2;
   uint32_t bq[KSTEPS][2];
-  {
+  auto read_inputs = [&] {
+    cur = st->cur_row;
+    for (int i = tid; i < nrows; i += kThreads) mask_s[i] = a.mask[(long long)b * R + r0 + i];
+    // score operand: the group's queries, lane l holding heads g = l / 4 (zero
+    // beyond G) at columns 16 kk + 2 (l % 4) + {0, 1} and + 8
     const uint32_t* qp = reinterpret_cast<const uint32_t*>(a.q + ((long long)b * a.q_heads + (long long)h * G + gq) * D);
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk) {
       bq[kk][0] = gq < G ? qp[kk * 8 + (lane & 3)] : 0u;
       bq[kk][1] = gq < G ? qp[kk * 8 + 4 + (lane & 3)] : 0u;
     }
-  }
-  // the step's new row, in the same round trip (only the owning CTA uses it)
-  if (append && tid < 2 * U) {
-    const int kv = tid >= U, u = kv ? tid - U : tid;
-    cp_async_16(smem_u32(sN) + tid * 16, (kv ? a.v_new : a.k_new) + ((long long)b * a.kv_heads + h) * D + u * 8);
-  }
+    // the step's new row, in the same round trip (only the owning CTA uses it)
+    if (append && tid < 2 * U) {
+      const int kv = tid >= U, u = kv ? tid - U : tid;
+      cp_async_16(smem_u32(sN) + tid * 16, (kv ? a.v_new : a.k_new) + ((long long)b * a.kv_heads + h) * D + u * 8);
+    }
+  };
+  const bool early = a.inputs_ready && append;
+  if (early) read_inputs();
+  pdl_wait();
+  if (!early) read_inputs();
   const bool state_ok = cur >= 0 && cur < R;
   const int cur_i = (append && state_ok) ? cur - r0 : -1;
   cp_async_wait_all();

@@ -121,6 +121,7 @@ struct DecodeArgs {
   const int32_t* valid_start;  // [B] left-pad counts (the cache's copy)
   int window;
   int ring;               // 1: modular ring cache (rows hold positions p - ((p - r) mod W))
+  int inputs_ready;       // 1: q, k_new, v_new, the mask and the state may be read before the launch wait
 };
 
 // SMs of the current device (cached per device; 152 if the query fails).

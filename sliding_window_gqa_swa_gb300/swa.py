@@ -73,6 +73,7 @@ _SIGS = {
     "swa_compact": (_I, [_P, _P, _P]),
     "swa_decode_workspace_bytes": (_SZ, [_P, _I]),
     "swa_decode": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, _P]),
+    "swa_decode_ex": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P, _SZ, ctypes.c_uint32, _P]),
     "swa_decode_noalloc": (_I, [_P, _I, _I, _P, _P, _P, _P, _F, _P, _P, _P]),
     "swa_roll": (_I, [_P, _P]),
     "swa_last_error": (ctypes.c_char_p, []),
@@ -317,10 +318,21 @@ def decode_workspace(cache: Cache, q_heads: int, device=None) -> torch.Tensor:
     return torch.zeros(decode_workspace_bytes(cache, q_heads), dtype=torch.uint8, device=dev)
 
 
+DECODE_INPUTS_READY = 1
+
+
 def decode(cache: Cache, layer: int, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
            mask: torch.Tensor, scale: float, out: torch.Tensor, workspace: torch.Tensor,
-           lse: Optional[torch.Tensor] = None, stream=None) -> None:
+           lse: Optional[torch.Tensor] = None, stream=None, inputs_ready: bool = False) -> None:
+    """swa_decode; ``inputs_ready`` calls swa_decode_ex with SWA_DECODE_INPUTS_READY
+    (the inputs were written before the previously enqueued kernel, which does
+    not write them: see include/swa.h)."""
     _bf16(q, "q")
+    if inputs_ready:
+        check(_lib.swa_decode_ex(cache.handle, layer, q.shape[-2], ptr(q), ptr(k_new), ptr(v_new), ptr(mask),
+                                 float(scale), ptr(out), ptr(lse), ptr(workspace), workspace.numel(),
+                                 DECODE_INPUTS_READY, stream_handle(stream)), "swa_decode_ex")
+        return
     check(_lib.swa_decode(cache.handle, layer, q.shape[-2], ptr(q), ptr(k_new), ptr(v_new), ptr(mask),
                           float(scale), ptr(out), ptr(lse), ptr(workspace), workspace.numel(),
                           stream_handle(stream)), "swa_decode")

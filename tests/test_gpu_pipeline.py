@@ -244,6 +244,74 @@ def test_graph_replay_matches_eager(swa, ring):
     assert np.array_equal(bits(results[False]), bits(results[True]))
 
 
+def test_inputs_ready_chain_under_graph(swa):
+    """SWA_DECODE_INPUTS_READY: with every layer's inputs of a step staged before
+    the step's mask, layers 1.. read them before waiting for the previous
+    layer's decode.  One captured graph per step (mask + three layers) replayed
+    across two rolls gives the same bits as plain decodes, and the oracle's
+    results."""
+    dev = torch.device("cuda")
+    L = 3
+    c = synth.decode_case(3300, batch=1, q_heads=4, kv_heads=2, head_dim=256, window=64, prompt_len=150,
+                          steps=130, layers=L)
+    S, W, D, B, Hq, Hkv = c.prompt_len, c.window, c.head_dim, c.batch, c.q_heads, c.kv_heads
+    scale = D ** -0.5
+    results = {}
+    for ready in (False, True):
+        pre = swa.Cache(swa.CACHE_PREFILL, L, B, Hkv, D, W, S)
+        for layer in range(L):
+            swa.prefill(pre, layer, swa.MODE_CAUSAL, torch.zeros(B, S, Hq, D, dtype=torch.bfloat16, device=dev),
+                        c.prompt_k[layer].to(dev), c.prompt_v[layer].to(dev), swa.Meta(B, S, 0, S, W), scale,
+                        torch.empty(B, S, Hq, D, dtype=torch.bfloat16, device=dev))
+        cache = swa.Cache(swa.CACHE_COMPACT, L, B, Hkv, D, W, S)
+        swa.compact(pre, cache)
+        mask = torch.empty(B, cache.rows, dtype=torch.uint8, device=dev)
+        ws = swa.decode_workspace(cache, Hq)
+        qb = torch.empty(L, B, Hq, D, dtype=torch.bfloat16, device=dev)
+        kb = torch.empty(L, B, Hkv, D, dtype=torch.bfloat16, device=dev)
+        vb = torch.empty_like(kb)
+        ob = torch.empty(L, B, Hq, D, dtype=torch.bfloat16, device=dev)
+
+        def step(stream=None):
+            swa.build_decode_mask(cache, mask, stream=stream)
+            for layer in range(L):
+                swa.decode(cache, layer, qb[layer], kb[layer], vb[layer], mask, scale, ob[layer], ws,
+                           stream=stream, inputs_ready=ready and layer > 0)
+
+        outs = []
+        graph = None
+        for t in range(c.steps):
+            if cache.needs_roll():
+                swa.roll(cache)
+            qb.copy_(c.dec_q[t])
+            kb.copy_(c.dec_k[t])
+            vb.copy_(c.dec_v[t])
+            if t == 0:
+                step()
+            elif graph is None:
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=s):
+                    step(stream=s)
+                torch.cuda.current_stream().wait_stream(s)
+                graph.replay()  # the capture advanced only the host mirror
+            else:
+                graph.replay()
+                cache.advance(1)
+            outs.append(ob.clone())
+        torch.cuda.synchronize()
+        cache.check()
+        results[ready] = torch.stack(outs)
+    assert np.array_equal(bits(results[False]), bits(results[True]))
+    check = [0, 1, 63, 64, 65, 127, 128, 129]
+    for layer in range(L):
+        ro, _ = reference.decode_full(c.prompt_k[layer], c.prompt_v[layer], c.dec_q[:, layer], c.dec_k[:, layer],
+                                      c.dec_v[:, layer], S, W, scale, steps=check)
+        for t in check:
+            assert_close(results[True][t, layer], ro[t], f"inputs-ready chain step {t} layer {layer}")
+
+
 def test_kv_sharing_layer(swa):
     """A KV-sharing layer (k_new = v_new = NULL) attends over the owning
     layer's rows, which already hold the step's token, and appends nothing."""
