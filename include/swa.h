@@ -350,18 +350,21 @@ SWA_API swa_status swa_decode(swa_cache* cache, int32_t layer, int32_t q_heads, 
 /* swa_decode with flags (0: exactly swa_decode; the decode itself is
  * [SPYRE] Summary's, the flag is library plumbing with no counterpart in the
  * pages).
- * SWA_DECODE_INPUTS_READY: q, k_new, v_new and the mask, and the cache state
- * the step's swa_build_mask set, were all written before the kernel enqueued
- * immediately before this call on the stream was enqueued, and that kernel
- * does not write them -- for example, the decodes of a step's layers when the
- * step's queries and new rows of every layer were produced before its
- * swa_build_mask, with each layer's call enqueued right after the previous
- * layer's.  The kernel then reads them before it waits for that previous
- * kernel (see "Launch chaining" above), which takes one round trip to global
- * memory off each layer's critical path.  Ignored by a KV-sharing call
- * (k_new = NULL) and by the batched-decode kernel (many slabs).  With the flag
- * and a previous kernel that does write one of them, results are undefined.
- * Other flag bits: SWA_EINVAL. */
+ * SWA_DECODE_INPUTS_READY: the caller guarantees that q, k_new, v_new, the
+ * mask and the cache state are complete in memory as soon as the kernel
+ * enqueued immediately before this call starts running, and that this kernel
+ * does not write them.  This holds for the decodes of a step's layers 1, 2, ...
+ * when the queries and new rows of every layer were produced before the
+ * step's swa_build_mask, each layer's call enqueued right after the previous
+ * layer's: the mask kernel lets no successor start before it has finished,
+ * the first layer's decode (called without the flag) waits for it, and each
+ * later layer's decode starts only after the previous one has started.  The
+ * kernel then reads those inputs before it waits for the previous kernel (see
+ * "Launch chaining" above; its compute and writes still follow that wait),
+ * which takes one round trip to global memory off each layer's critical path.
+ * Ignored by a KV-sharing call (k_new = NULL) and by the batched-decode kernel
+ * (many slabs).  With the flag and inputs that are not complete when the
+ * previous kernel starts, results are undefined.  Other flag bits: SWA_EINVAL. */
 SWA_API swa_status swa_decode_ex(swa_cache* cache, int32_t layer, int32_t q_heads, const swa_bf16* q,
                                  const swa_bf16* k_new, const swa_bf16* v_new, const uint8_t* mask,
                                  float scale, swa_bf16* out, float* lse, void* workspace,
