@@ -153,6 +153,19 @@ def test_decode_shapes_with_padding(swa, batch, hq, hkv, d, w, s):
     assert_lse(dec_l, ref_l, "decode lse")
 
 
+# The throughput regime (at least as many (sequence, KV head) slabs as SMs):
+# eight compute warps per CTA, a few row-range splits per slab merged through
+# the workspace.  Sequences of every length from one prompt token up (left
+# padding filled with large finite garbage), so some splits admit no row and
+# some a single one, across a roll; head sizes 64 to 512, groups of 1 to 8.
+def test_throughput_regime_length_mix(swa, batch, hq, hkv, d, w, s):
+    c = synth.decode_case(3600 + d + hq, batch=batch, q_heads=hq, kv_heads=hkv, head_dim=d, window=w,
+                          prompt_len=s, steps=70, layers=1, with_prompt_q=False, lengths=(1, s), garbage=50.0)
+    _, _, dec_o, dec_l, ref_o, ref_l = run_decode_case(swa, c, check_every_step=False)
+    assert_close(dec_o, ref_o, "decode")
+    assert_lse(dec_l, ref_l, "decode lse")
+
+
 def test_workload1_ring(swa):
     c = synth.workload1()
     _, _, dec_o, dec_l, ref_o, ref_l = run_decode_case(swa, c, ring=True)
