@@ -158,6 +158,9 @@ def test_decode_shapes_with_padding(swa, batch, hq, hkv, d, w, s):
 # the workspace.  Sequences of every length from one prompt token up (left
 # padding filled with large finite garbage), so some splits admit no row and
 # some a single one, across a roll; head sizes 64 to 512, groups of 1 to 8.
+@pytest.mark.parametrize("batch,hq,hkv,d,w,s", [(40, 8, 4, 256, 64, 150), (20, 16, 8, 128, 256, 300),
+                                                (160, 2, 1, 512, 128, 200), (40, 32, 4, 64, 128, 140),
+                                                (80, 2, 2, 256, 256, 400)])
 def test_throughput_regime_length_mix(swa, batch, hq, hkv, d, w, s):
     c = synth.decode_case(3600 + d + hq, batch=batch, q_heads=hq, kv_heads=hkv, head_dim=d, window=w,
                           prompt_len=s, steps=70, layers=1, with_prompt_q=False, lengths=(1, s), garbage=50.0)
