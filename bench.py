@@ -259,13 +259,16 @@ class SingleStreamJob:
         self.meta = swa.Meta(self.B, self.S, 0, self.S, self.W)
         self.mask = torch.empty(self.B, self.cmp.rows, dtype=torch.uint8, device=dev)
         self.ws = swa.decode_workspace(self.cmp, self.Hq)
-        # staging buffers the captured step graph reads (views of one buffer) and writes
-        self.stage = torch.empty(self.nq + 2 * self.nk, dtype=torch.bfloat16, device=dev)
-        self.qb = self.stage[:self.nq].view(self.L, self.B, self.Hq, self.D)
-        self.kb = self.stage[self.nq:self.nq + self.nk].view(self.L, self.B, self.Hkv, self.D)
-        self.vb = self.stage[self.nq + self.nk:].view(self.L, self.B, self.Hkv, self.D)
-        self.ob = torch.empty((self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
-        self.graph = None
+        # staging buffers the captured step graph reads (views of one buffer) and writes: two
+        # sets (one graph each, steps alternate), so a copy stream stages the next step's inputs
+        # and stores the previous step's outputs while a step runs; one set, copied in line,
+        # when L2 is flushed before every step (that variant times each step's graph alone)
+        self.nbuf = 1 if l2_flush is not None else 2
+        self.stage = [torch.empty(self.nq + 2 * self.nk, dtype=torch.bfloat16, device=dev) for _ in range(self.nbuf)]
+        self.ob = [torch.empty((self.L, self.B, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
+                   for _ in range(self.nbuf)]
+        self.graphs = [None] * self.nbuf
+        self.copy_stream = torch.cuda.Stream(dev) if self.nbuf == 2 else None
         self.rolls = 0 if ring else (self.T - 1) // 64
         # kernels of ours per job: 2 cache bindings, (K/V write + attention) per layer, compaction,
         # (mask + one decode per layer) per step, rolls
@@ -274,8 +277,15 @@ class SingleStreamJob:
                           + self.dec.numel()) * 2 if e2e else 0
         self.d2h_bytes = self.outs.numel() * 2 if e2e else 0
 
-    def _capture(self):
+    def _views(self, i):
+        st = self.stage[i]
+        return (st[:self.nq].view(self.L, self.B, self.Hq, self.D),
+                st[self.nq:self.nq + self.nk].view(self.L, self.B, self.Hkv, self.D),
+                st[self.nq + self.nk:].view(self.L, self.B, self.Hkv, self.D))
+
+    def _capture(self, i):
         swa = self.swa
+        qb, kb, vb = self._views(i)
         s = torch.cuda.Stream(self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
         g = torch.cuda.CUDAGraph()
@@ -285,10 +295,19 @@ class SingleStreamJob:
                 # the step's inputs of every layer are staged before the mask kernel, so from
                 # layer 1 on the kernel launched just before (the previous layer's decode) writes
                 # none of them: SWA_DECODE_INPUTS_READY
-                swa.decode(self.cmp, layer, self.qb[layer], self.kb[layer], self.vb[layer], self.mask,
-                           self.scale, self.ob[layer], self.ws, stream=s, inputs_ready=layer > 0)
+                swa.decode(self.cmp, layer, qb[layer], kb[layer], vb[layer], self.mask,
+                           self.scale, self.ob[i][layer], self.ws, stream=s, inputs_ready=layer > 0)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         return g
+
+    def _replay(self, i):
+        if self.graphs[i] is None:
+            self.graphs[i] = self._capture(i)
+            # the capture advanced the host mirror once; this replay advances the device
+            self.graphs[i].replay()
+        else:
+            self.graphs[i].replay()
+            self.cmp.advance(1)
 
     def make_events(self):
         return {"start": ev(), "inputs": ev(), "prefill": ev(), "decode_start": ev(), "end": ev(),
@@ -310,23 +329,57 @@ class SingleStreamJob:
         e["prefill"].record()
         swa.compact(self.pre, self.cmp)
         e["decode_start"].record()
+        if self.nbuf == 2:
+            self._decode_steps_overlapped(e)
+        else:
+            for t in range(self.T):
+                if self.cmp.needs_roll():
+                    swa.roll(self.cmp)
+                self.stage[0].copy_(self.dec[t], non_blocking=True)
+                if self.l2_flush is not None:
+                    self.l2_flush.fill_(t & 127)
+                e["step_s"][t].record()
+                self._replay(0)
+                e["step_e"][t].record()
+                self.outs[t].copy_(self.ob[0], non_blocking=True)
+        e["end"].record()
+
+    def _decode_steps_overlapped(self, e):
+        """The decode steps: step t uses staging set t % 2.  On the copy stream the copy of step
+        t + 1's inputs into its set (after step t - 1, the set's last reader) and the copy of step
+        t's outputs out of its set run while the compute stream replays the next graph; end to
+        end these are the host uploads and downloads."""
+        swa, cs = self.swa, self.copy_stream
+        main = torch.cuda.current_stream(self.dev)
+        up = [torch.cuda.Event() for _ in range(2)]    # inputs of the set landed
+        done = [torch.cuda.Event() for _ in range(2)]  # the set's graph finished
+        down = [torch.cuda.Event() for _ in range(2)]  # the set's outputs left
+        cs.wait_stream(main)
+        with torch.cuda.stream(cs):
+            self.stage[0].copy_(self.dec[0], non_blocking=True)
+            up[0].record(cs)
         for t in range(self.T):
+            i = t % 2
+            if t + 1 < self.T:
+                with torch.cuda.stream(cs):
+                    if t >= 1:
+                        cs.wait_event(done[1 - i])
+                    self.stage[1 - i].copy_(self.dec[t + 1], non_blocking=True)
+                    up[1 - i].record(cs)
             if self.cmp.needs_roll():
                 swa.roll(self.cmp)
-            self.stage.copy_(self.dec[t], non_blocking=True)
-            if self.l2_flush is not None:
-                self.l2_flush.fill_(t & 127)
+            main.wait_event(up[i])
+            if t >= 2:
+                main.wait_event(down[i])
             e["step_s"][t].record()
-            if self.graph is None:
-                self.graph = self._capture()
-                # the capture advanced the host mirror once; this replay advances the device
-                self.graph.replay()
-            else:
-                self.graph.replay()
-                self.cmp.advance(1)
+            self._replay(i)
             e["step_e"][t].record()
-            self.outs[t].copy_(self.ob, non_blocking=True)
-        e["end"].record()
+            done[i].record(main)
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[i])
+                self.outs[t].copy_(self.ob[i], non_blocking=True)
+                down[i].record(cs)
+        main.wait_stream(cs)
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -401,7 +454,8 @@ def run_ours(args):
                "h2d_bytes_per_step": int(ejob.h2d_bytes), "d2h_bytes_per_step": int(ejob.d2h_bytes),
                "job_ms": round(sum(e["start"].elapsed_time(e["end"]) for e in eev) / args.steps, 3),
                "note": "per decode step: H2D of that step's q/k/v for 26 layers from pinned memory and D2H of "
-                       "its outputs, inside the decode phase; the prompt upload is inside job_ms"}
+                       "its outputs, inside the decode phase, on a copy stream overlapping the neighbouring "
+                       "steps' graphs; the prompt upload is inside job_ms"}
         del ejob
         torch.cuda.empty_cache()
 
@@ -473,7 +527,9 @@ def run_ours(args):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "decode_chaining": "one step graph: the shared mask, then the 26 layers' decodes chained by "
                                       "programmatic launch; the step's inputs of all layers are staged before "
-                                      "the mask, so layers 1-25 use SWA_DECODE_INPUTS_READY"},
+                                      "the mask, so layers 1-25 use SWA_DECODE_INPUTS_READY",
+                   "staging": "two staging sets, steps alternate: a copy stream stages step t+1's inputs and "
+                              "stores step t-1's outputs while step t's graph runs (inside the timed region)"},
         "decode_us_per_layer": round(us_per_layer, 4),
         "decode_launch_us": round(launch_us, 4),
         "prefill_ms_per_job": round(prefill_ms / args.steps, 3),
